@@ -1,0 +1,523 @@
+#!/usr/bin/env python
+"""Benchmark of the DCP LSE-weighted merge on GB300.
+
+Metric: LSE-combine HBM GB/s (and % of the HBM roofline) and us/call at batch
+rows 1-128, one GB300. Workload: Kimi-K2.5 geometry (cp = 4, 64 heads, 16 per
+destination, D = 512, bf16 partials, base-2 fp32 LSEs U[-4, 24]) swept over
+rows 1, 8, 16, 32, 64, 128.
+
+One step = one pass of the whole merge over every row count of the sweep:
+for each row count, one replay of a CUDA graph holding 60 calls (the pages'
+per-layer microbenchmark method: "[DCP] Run fi_a2a on FlashInfer's fused
+all-to-all + LSE reduce", "Speed Tests and Profiling"). Each of the 60 calls
+reads and writes its own buffers, and L2 is flushed (a write larger than L2)
+before every step, so every call starts cold and the GB/s are HBM GB/s.
+Steps are timed with CUDA events on the launching stream; the flush sits
+outside the events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas: the merge has no exchange step on one node here),
+the time is the max over ranks and the value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "LSE-combine HBM GB/s (% of peak) and µs/call at rows 1–128, 1×GB300"
+CALLS_PER_GRAPH = 60
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCE = os.path.join(ROOT, "decode_context_mla_dcp_gb300", "csrc", "dcp_lse_reduce.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+# ---------------------------------------------------------------------------- utilities
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate_ranks(local_seconds: float, local_bytes: float, group=None):
+    """Max of the timed-region seconds and sum of the bytes over all ranks
+    (the whole-job figures). With one process this is the identity."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size(group) == 1:
+        return local_seconds, local_bytes
+    backend = dist.get_backend(group)
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    b = torch.tensor([local_bytes], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(b.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, only if it was
+    taken on the kernel source as it is now."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha256") != kernel_source_sha():
+        return None
+    return d.get("per_launch_bytes_bench_step")
+
+
+class ClockSampler:
+    """nvidia-smi samples of this GPU's clocks and throttle reasons."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and parts[0] != self.uuid:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------- the workload
+
+def workload_config():
+    from decode_context_mla_dcp_gb300.inputs import CONFIGS
+    return CONFIGS["kimi"]
+
+
+def sweep_bytes(cfg):
+    from decode_context_mla_dcp_gb300 import algorithmic_bytes
+    return {rows: algorithmic_bytes(cfg.cp, rows, cfg.H, cfg.D) for rows in cfg.rows}
+
+
+class RowSet:
+    """Device buffers for one row count: `slots` independent copies of the
+    inputs and outputs, so consecutive calls never share cache lines."""
+
+    def __init__(self, cfg, rows: int, slots: int, seed: int = 0):
+        import torch
+        from decode_context_mla_dcp_gb300.inputs import make_merge_inputs
+        self.cfg, self.rows, self.slots = cfg, rows, slots
+        self.inp = make_merge_inputs(cfg, rows, seed=seed)
+        cp, H, D, Hl = cfg.cp, cfg.H, cfg.D, cfg.H // cfg.cp
+        self.src = []
+        self.lse = []
+        for j in range(cp):
+            s = torch.from_numpy(self.inp.srcs[j].view(np.int16)).view(torch.bfloat16).cuda()
+            l = torch.from_numpy(self.inp.lses[j]).cuda()
+            self.src.append(s.unsqueeze(0).repeat(slots, 1, 1, 1).contiguous())
+            self.lse.append(l.unsqueeze(0).repeat(slots, 1, 1).contiguous())
+        self.dst = [torch.empty((slots, rows, Hl, D), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
+        self.lse_out = [torch.empty((slots, rows, Hl), dtype=torch.float32, device="cuda") for _ in range(cp)]
+
+    def ptrs(self, k: int):
+        return ([s[k].data_ptr() for s in self.src], [l[k].data_ptr() for l in self.lse],
+                [d[k].data_ptr() for d in self.dst], [l[k].data_ptr() for l in self.lse_out])
+
+    def call(self, k: int, flags: int):
+        import decode_context_mla_dcp_gb300 as dcp
+        src, lse, dst, lout = self.ptrs(k)
+        c = self.cfg
+        dcp.dcp_lse_reduce_ex(src, lse, c.cp, self.rows, c.H, c.D, c.lse_base_e, dcp.DCP_DTYPE_BF16, dst, lout,
+                              flags=flags)
+
+    def capture(self, flags: int, same_slot: bool = False):
+        import torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.call(0, flags)  # warm-up outside the capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for k in range(CALLS_PER_GRAPH):
+                self.call(0 if same_slot else k % self.slots, flags)
+        return g
+
+
+def time_graphs(graphs, reps: int, flush=None):
+    """Median us per call of each graph over `reps` replays (events on the
+    current stream; optional L2 flush before each replay, outside the events)."""
+    import torch
+    out = {}
+    for key, g in graphs.items():
+        times = []
+        for _ in range(reps):
+            if flush is not None:
+                flush.add_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e3 / CALLS_PER_GRAPH)
+        out[key] = statistics.median(times)
+    return out
+
+
+def stress_extra(peak):
+    """Bandwidth-stress config (cp=8, 128 heads, D=512, 4096 rows, base-e LSE
+    U[0, 30]): 4.85 GB per call, cold by size. Inputs drawn on the device with
+    a seeded torch generator (same laws as the host generator; timing only)."""
+    import torch
+    import decode_context_mla_dcp_gb300 as dcp
+    cp, H, D, B = 8, 128, 512, 4096
+    Hl = H // cp
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    src = [torch.randn((B, H, D), generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+           for _ in range(cp)]
+    lse = [torch.rand((B, H), generator=gen, device="cuda") * 30.0 for _ in range(cp)]
+    dst = [torch.empty((B, Hl, D), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
+    lout = [torch.empty((B, Hl), dtype=torch.float32, device="cuda") for _ in range(cp)]
+
+    def call():
+        dcp.dcp_lse_reduce_ex(src, lse, cp, B, H, D, True, dcp.DCP_DTYPE_BF16, dst, lout, flags=dcp.DCP_FLAG_PDL)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(15):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(4):
+            call()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1e3 / 4)
+    us = statistics.median(times)
+    nbytes = dcp.algorithmic_bytes(cp, B, H, D)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del src, lse, dst, lout
+    torch.cuda.empty_cache()
+    return {"workload": "bandwidth stress: cp=8, H=128, D=512, rows=4096, bf16, base-e LSE U[0,30]",
+            "us_per_call": round(us, 2), "bytes_per_call": nbytes, "gbs": round(gbs, 1),
+            "frac_of_measured_peak": round(gbs / peak, 4)}
+
+
+def e2e_measure(cfg, steps: int):
+    """The same metric end to end through the public API: every step copies
+    each row count's inputs from pinned host memory, merges, and reads the
+    merged outputs and LSEs back into pinned host memory."""
+    import torch
+    import decode_context_mla_dcp_gb300 as dcp
+    from decode_context_mla_dcp_gb300.inputs import make_merge_inputs
+    sets = []
+    h2d = d2h = 0
+    nbytes = 0
+    for rows in cfg.rows:
+        inp = make_merge_inputs(cfg, rows, seed=0)
+        hs = [torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).pin_memory() for s in inp.srcs]
+        hl = [torch.from_numpy(l).pin_memory() for l in inp.lses]
+        ds = [torch.empty_like(t, device="cuda") for t in hs]
+        dl = [torch.empty_like(t, device="cuda") for t in hl]
+        Hl = cfg.H // cfg.cp
+        do = [torch.empty((rows, Hl, cfg.D), dtype=torch.bfloat16, device="cuda") for _ in range(cfg.cp)]
+        dlo = [torch.empty((rows, Hl), dtype=torch.float32, device="cuda") for _ in range(cfg.cp)]
+        ho = [torch.empty_like(t, device="cpu").pin_memory() for t in do]
+        hlo = [torch.empty_like(t, device="cpu").pin_memory() for t in dlo]
+        sets.append((rows, hs, hl, ds, dl, do, dlo, ho, hlo))
+        h2d += sum(t.numel() * t.element_size() for t in hs + hl)
+        d2h += sum(t.numel() * t.element_size() for t in ho + hlo)
+        nbytes += dcp.algorithmic_bytes(cfg.cp, rows, cfg.H, cfg.D)
+
+    def step():
+        for rows, hs, hl, ds, dl, do, dlo, ho, hlo in sets:
+            for d, h in zip(ds + dl, hs + hl):
+                d.copy_(h, non_blocking=True)
+            dcp.dcp_lse_reduce(ds, dl, cfg.H, cfg.cp, rows, cfg.H, cfg.D, cfg.lse_base_e, do, dlo)
+            for h, d in zip(ho + hlo, do + dlo):
+                h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    b.synchronize()
+    sec = a.elapsed_time(b) * 1e-3
+    tot_sec, tot_bytes = aggregate_ranks(sec, float(nbytes * steps))
+    return {"value": round(tot_bytes / tot_sec / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(tot_sec * 1e3 / steps, 4),
+            "how": "pinned host -> device copies, dcp_lse_reduce, device -> pinned host copies for each row count, "
+                   "eager, timed with CUDA events"}
+
+
+def cpu_baseline(cfg, budget_s: float = 12.0):
+    """The CPU oracle as it stands (single-threaded fp64 C), on the sweep's
+    inputs, repeated until about `budget_s` seconds of CPU work."""
+    import oracle
+    from decode_context_mla_dcp_gb300 import algorithmic_bytes
+    from decode_context_mla_dcp_gb300.inputs import make_merge_inputs
+    oracle.build()
+    inputs = [make_merge_inputs(cfg, rows, seed=0) for rows in cfg.rows]
+    per_pass = sum(algorithmic_bytes(cfg.cp, i.B, cfg.H, cfg.D) for i in inputs)
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        for inp in inputs:
+            oracle.merge(inp.srcs, inp.lses, inp.lse_base_e)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(per_pass * passes / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{passes} passes over the rows {list(cfg.rows)} sweep ({per_pass} algorithmic bytes each), "
+                      f"{el:.1f} s, single-threaded fp64 C"}
+
+
+# ---------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from decode_context_mla_dcp_gb300 import algorithmic_bytes
+    from decode_context_mla_dcp_gb300.inputs import make_merge_inputs
+    cfg = workload_config()
+    oracle.build()
+    inputs = [make_merge_inputs(cfg, rows, seed=0) for rows in cfg.rows]
+    per_step = sum(algorithmic_bytes(cfg.cp, i.B, cfg.H, cfg.D) for i in inputs)
+
+    def step():
+        for inp in inputs:
+            oracle.merge(inp.srcs, inp.lses, inp.lse_base_e)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    sec = time.perf_counter() - t0
+    value = per_step * args.steps / sec / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(cfg),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step = one pass of the fp64 C oracle over rows {list(cfg.rows)}"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(cfg):
+    return {"workload": f"{cfg.name} DCP LSE merge: cp={cfg.cp}, H={cfg.H} ({cfg.H // cfg.cp} per destination), "
+                        f"D={cfg.D}, bf16 partials N(0,1), base-2 fp32 LSE U[-4,24], rows {list(cfg.rows)}",
+            "cp": cfg.cp, "heads": cfg.H, "head_dim": cfg.D, "rows": list(cfg.rows),
+            "calls_per_graph": CALLS_PER_GRAPH,
+            "l2": "flushed before every step (write of 4x L2); each of a graph's 60 calls has its own buffers",
+            "parallelism": "replicas (one independent merge workload per GPU)"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import decode_context_mla_dcp_gb300 as dcp
+    from decode_context_mla_dcp_gb300 import build as dcp_build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dcp_build.build()
+    dcp.load()
+    cfg = workload_config()
+    peak, peak_kind = measured_peaks()
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or (126 << 20)
+    flush = torch.zeros((max(4 * l2, 512 << 20) // 4,), dtype=torch.float32, device="cuda")
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+
+    flags = dcp.DCP_FLAG_PDL
+    bytes_per_rows = sweep_bytes(cfg)
+    step_bytes = sum(bytes_per_rows.values()) * CALLS_PER_GRAPH
+    sets = {rows: RowSet(cfg, rows, CALLS_PER_GRAPH) for rows in cfg.rows}
+    graphs = {rows: sets[rows].capture(flags) for rows in cfg.rows}
+    torch.cuda.synchronize()
+
+    def step(record=None):
+        flush.add_(1.0)  # evict L2 (outside the step's events)
+        if record is not None:
+            record[0].record()
+        for i, rows in enumerate(cfg.rows):
+            graphs[rows].replay()
+            if record is not None:
+                record[i + 1].record()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(cfg.rows) + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        step(evs[k])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+
+    step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)]
+    per_rows_us = {rows: statistics.median(evs[k][i].elapsed_time(evs[k][i + 1]) * 1e3 / CALLS_PER_GRAPH
+                                           for k in range(args.steps))
+                   for i, rows in enumerate(cfg.rows)}
+    local_sec = sum(step_ms) * 1e-3
+    tot_sec, tot_bytes = aggregate_ranks(local_sec, step_bytes * args.steps)
+    value = tot_bytes / tot_sec / 1e9
+    achieved = step_bytes * args.steps / local_sec / 1e9
+
+    out = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(tot_sec * 1e3 / args.steps, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic", "config": config_dict(cfg),
+           "wall_ms_per_step": round(wall * 1e3 / args.steps, 4),
+           "gpu_launches": args.steps * len(cfg.rows) * CALLS_PER_GRAPH,
+           "sweep": {str(rows): {"us_per_call": round(per_rows_us[rows], 3), "bytes_per_call": bytes_per_rows[rows],
+                                 "gbs": round(bytes_per_rows[rows] / (per_rows_us[rows] * 1e-6) / 1e9, 1),
+                                 "frac_of_measured_peak": round(bytes_per_rows[rows] / (per_rows_us[rows] * 1e-6)
+                                                                / 1e9 / peak, 4)}
+                     for rows in cfg.rows},
+           "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(achieved / peak, 4), "traffic": recorded_traffic(),
+                        "peak_kind": f"{peak_kind} (burst copy bandwidth)",
+                        "per_unit": "algorithmic bytes per call = cp*B*H*D*2 + cp*B*H*4 + B*H*D*2 + B*H*4",
+                        "bytes_per_launch_avg": step_bytes / (len(cfg.rows) * CALLS_PER_GRAPH)},
+           "clocks": clocks}
+
+    if rank == 0 and not args.no_extras:
+        hot = {rows: sets[rows].capture(flags, same_slot=True) for rows in cfg.rows}
+        nopdl = {rows: sets[rows].capture(0) for rows in cfg.rows}
+        hot_us = time_graphs(hot, 20)
+        cold_nopdl_us = time_graphs(nopdl, 20, flush=flush)
+        out["extras"] = {
+            "l2_hot_us_per_call": {str(r): round(v, 3) for r, v in hot_us.items()},
+            "cold_no_pdl_us_per_call": {str(r): round(v, 3) for r, v in cold_nopdl_us.items()},
+        }
+        del hot, nopdl
+    out["e2e"] = e2e_measure(cfg, max(10, min(args.steps, 100)))
+    if rank == 0 and not args.no_extras:
+        del sets, graphs
+        torch.cuda.empty_cache()
+        out["extras"]["largest_config"] = stress_extra(peak)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="skip the L2-hot, no-PDL and stress extras")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

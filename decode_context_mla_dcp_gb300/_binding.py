@@ -1,0 +1,140 @@
+"""ctypes binding of the C ABI in include/dcp_lse_reduce.h.
+
+Argument marshalling only: every step of the merge runs in the sm_103a kernel.
+Pointers may be given as integers or as torch tensors (their data_ptr()); a
+stream may be None (torch's current stream), an integer cudaStream_t or a
+torch.cuda.Stream. A nonzero status raises DcpError carrying the library's
+message. There is no fallback: if the library is not built, the first call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+DCP_LSE_REDUCE_CP_MAX = 16
+DCP_DTYPE_BF16 = 0
+DCP_DTYPE_F16 = 1
+DCP_FLAG_PDL = 1
+DCP_FLAG_PRELOAD = 2
+DCP_FLAG_LSE_FIRST = 4
+
+EXPORTED_SYMBOLS = ("dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dcp_lse_reduce_version")
+
+
+class DcpError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"dcp_lse_reduce failed ({status}): {message}")
+        self.status = status
+
+
+class Layout(ctypes.Structure):
+    """Strides in elements; mirrors dcp_lse_reduce_layout."""
+    _fields_ = [("src_row", ctypes.c_int64), ("src_head", ctypes.c_int64),
+                ("lse_row", ctypes.c_int64), ("lse_head", ctypes.c_int64),
+                ("dst_row", ctypes.c_int64), ("dst_head", ctypes.c_int64),
+                ("lse_out_row", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Open the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"the sm_103a library is not built ({p} missing): run "
+                "`python -m decode_context_mla_dcp_gb300.build` or __graft_entry__.build()")
+        lib = ctypes.CDLL(p)
+        vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.dcp_lse_reduce.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i64, ci, i64, ci, ci, ci,
+                                       ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
+        lib.dcp_lse_reduce.restype = ci
+        lib.dcp_lse_reduce_ex.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ci, i64, ci, ci, ci, ci,
+                                          ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(Layout),
+                                          ctypes.c_uint, vp]
+        lib.dcp_lse_reduce_ex.restype = ci
+        lib.dcp_lse_reduce_strerror.argtypes = [ci]
+        lib.dcp_lse_reduce_strerror.restype = ctypes.c_char_p
+        lib.dcp_lse_reduce_version.argtypes = []
+        lib.dcp_lse_reduce_version.restype = ci
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _ptr_array(xs, n: int, allow_none: bool = False):
+    if xs is None:
+        if allow_none:
+            return None
+        raise ValueError("pointer array is required")
+    vals = [_ptr(x) for x in xs]
+    if len(vals) < n:
+        raise ValueError(f"need {n} pointers, got {len(vals)}")
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise DcpError(status, dcp_lse_reduce_strerror(status))
+
+
+def dcp_lse_reduce(src_ptrs, lse_ptrs, lse_stride: int, cp: int, B: int, H: int, D: int, lse_base_e: bool,
+                   dst_ptrs, lse_out_ptrs=None, stream=None) -> None:
+    """The merge over contiguous [B, H, D] bf16 buffers (see the C header)."""
+    lib = load()
+    _check(lib.dcp_lse_reduce(_ptr_array(src_ptrs, cp), _ptr_array(lse_ptrs, cp), int(lse_stride), int(cp),
+                              int(B), int(H), int(D), 1 if lse_base_e else 0, _ptr_array(dst_ptrs, cp),
+                              _ptr_array(lse_out_ptrs, cp, allow_none=True), _stream(stream)))
+
+
+def dcp_lse_reduce_ex(src_ptrs, lse_ptrs, cp: int, B: int, H: int, D: int, lse_base_e: bool,
+                      dtype: int, dst_ptrs, lse_out_ptrs=None, layout: Layout | dict | None = None,
+                      flags: int = 0, stream=None) -> None:
+    """The merge with explicit strides, dtype and launch flags (see the C header)."""
+    lib = load()
+    if isinstance(layout, dict):
+        layout = Layout(**layout)
+    _check(lib.dcp_lse_reduce_ex(_ptr_array(src_ptrs, cp), _ptr_array(lse_ptrs, cp), int(cp), int(B), int(H),
+                                 int(D), 1 if lse_base_e else 0, int(dtype), _ptr_array(dst_ptrs, cp),
+                                 _ptr_array(lse_out_ptrs, cp, allow_none=True),
+                                 ctypes.byref(layout) if layout is not None else None, int(flags),
+                                 _stream(stream)))
+
+
+def dcp_lse_reduce_strerror(status: int) -> str:
+    return load().dcp_lse_reduce_strerror(int(status)).decode()
+
+
+def dcp_lse_reduce_version() -> int:
+    return int(load().dcp_lse_reduce_version())

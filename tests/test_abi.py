@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+function include/dcp_lse_reduce.h declares, and bad arguments are rejected on
+the host with the documented status (no GPU needed: nothing is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import decode_context_mla_dcp_gb300 as dcp
+from decode_context_mla_dcp_gb300 import build as dcp_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dcp_lse_reduce.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dcp_build.build()
+    return dcp.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(dcp_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_exported_api():
+    assert declared_functions() == sorted(dcp.EXPORTED_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_messages(lib):
+    assert dcp.dcp_lse_reduce_version() == 10000
+    assert "multiple of cp" in dcp.dcp_lse_reduce_strerror(-4)
+    assert dcp.dcp_lse_reduce_strerror(0) == "success"
+
+
+FAKE = 1 << 20  # a 16-byte-aligned non-null address; never dereferenced on the host
+
+
+def call(lib, cp=2, B=1, H=4, D=512, lse_stride=None, srcs=None, lses=None, dsts=None, lse_outs=None,
+         base_e=1):
+    arr = ctypes.c_void_p * max(cp, 1)
+    srcs = arr(*([FAKE] * max(cp, 1))) if srcs is None else srcs
+    lses = arr(*([FAKE] * max(cp, 1))) if lses is None else lses
+    dsts = arr(*([FAKE + 4096] * max(cp, 1))) if dsts is None else dsts
+    return lib.dcp_lse_reduce(srcs, lses, H if lse_stride is None else lse_stride, cp, B, H, D, base_e,
+                              dsts, lse_outs, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(cp=0), -2), (dict(cp=17, H=17), -2), (dict(B=-1), -3), (dict(H=0), -3),
+    (dict(D=0), -3), (dict(D=12), -3), (dict(H=6, cp=4), -4), (dict(lse_stride=3), -5),
+])
+def test_bad_arguments_are_rejected(lib, kw, status):
+    assert call(lib, **kw) == status
+
+
+def test_null_pointers_are_rejected(lib):
+    arr = ctypes.c_void_p * 2
+    assert lib.dcp_lse_reduce(None, arr(FAKE, FAKE), 4, 2, 1, 4, 512, 1, arr(FAKE, FAKE), None, None) == -1
+    assert call(lib, srcs=arr(FAKE, 0)) == -1
+    assert call(lib, dsts=arr(0, FAKE)) == -1
+
+
+def test_misaligned_pointers_are_rejected(lib):
+    arr = ctypes.c_void_p * 2
+    assert call(lib, srcs=arr(FAKE, FAKE + 8)) == -6
+    assert call(lib, dsts=arr(FAKE + 2, FAKE)) == -6
+    assert call(lib, lses=arr(FAKE + 2, FAKE)) == -6
+    assert call(lib, lse_outs=arr(FAKE + 1, 0)) == -6
+
+
+def test_empty_batch_is_a_no_op(lib):
+    # B = 0 returns before touching the device
+    assert call(lib, B=0) == 0
+
+
+def test_ex_rejects_bad_flags_dtype_strides(lib):
+    arr = ctypes.c_void_p * 2
+    p = arr(FAKE, FAKE)
+    q = arr(FAKE + 4096, FAKE + 4096)
+
+    def ex(dtype=0, flags=0, layout=None, base_e=1):
+        return lib.dcp_lse_reduce_ex(p, p, 2, 1, 4, 512, base_e, dtype, q, None,
+                                     ctypes.byref(layout) if layout is not None else None, flags, None)
+
+    assert ex(dtype=2) == -8
+    assert ex(base_e=2) == -9
+    assert ex(flags=8) == -7
+    assert ex(flags=dcp.DCP_FLAG_PRELOAD | dcp.DCP_FLAG_LSE_FIRST) == -7
+    good = dict(src_row=2048, src_head=512, lse_row=4, lse_head=1, dst_row=1024, dst_head=512, lse_out_row=2)
+    for key, bad in [("src_row", 2044), ("src_head", 4), ("dst_row", -8), ("dst_head", 12), ("lse_row", -1)]:
+        lay = dcp.Layout(**{**good, key: bad})
+        assert ex(layout=lay) == -5, key
+
+
+def test_python_binding_raises_with_message(lib):
+    with pytest.raises(dcp.DcpError, match="multiple of cp"):
+        dcp.dcp_lse_reduce([FAKE] * 4, [FAKE] * 4, 6, 4, 1, 6, 512, True, [FAKE] * 4, stream=0)
