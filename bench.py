@@ -503,6 +503,40 @@ def run_ours(args):
     return 0
 
 
+def run_case(args):
+    """A few plain calls of one config, for ncu captures: `--case NAME
+    --rows R1,R2,... --calls N` calls the merge N times per row count, each
+    call on its own buffers, with no graph and no timing."""
+    import torch
+    import decode_context_mla_dcp_gb300 as dcp
+    from decode_context_mla_dcp_gb300 import build as dcp_build
+    from decode_context_mla_dcp_gb300.inputs import CONFIGS, make_merge_inputs
+    torch.cuda.set_device(dist_env()[2])
+    dcp_build.build()
+    cfg = CONFIGS[args.case]
+    rows_list = [int(r) for r in args.rows.split(",")] if args.rows else list(cfg.rows)
+    flags = dcp.DCP_FLAG_PDL
+    for rows in rows_list:
+        inp = make_merge_inputs(cfg, rows, seed=0)
+        Hl = cfg.H // cfg.cp
+        sets = []
+        for _ in range(args.calls):
+            src = [torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).cuda() for s in inp.srcs]
+            lse = [torch.from_numpy(l).cuda() for l in inp.lses]
+            dst = [torch.empty((rows, Hl, cfg.D), dtype=torch.bfloat16, device="cuda") for _ in range(cfg.cp)]
+            lout = [torch.empty((rows, Hl), dtype=torch.float32, device="cuda") for _ in range(cfg.cp)]
+            sets.append((src, lse, dst, lout))
+        torch.cuda.synchronize()
+        for src, lse, dst, lout in sets:
+            dcp.dcp_lse_reduce_ex(src, lse, cfg.cp, rows, cfg.H, cfg.D, cfg.lse_base_e, dcp.DCP_DTYPE_BF16,
+                                  dst, lout, flags=flags)
+        torch.cuda.synchronize()
+        del sets
+        torch.cuda.empty_cache()
+    print(f"case {args.case} rows {rows_list} x {args.calls} calls done", flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -511,7 +545,13 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the L2-hot, no-PDL and stress extras")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["kimi", "deepseek", "spec", "stress"],
+                    help="profiling mode: plain calls of one config, no timing")
+    ap.add_argument("--rows", default="", help="with --case: comma-separated row counts")
+    ap.add_argument("--calls", type=int, default=3, help="with --case: calls per row count")
     args = ap.parse_args(argv)
+    if args.case:
+        return run_case(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
