@@ -41,24 +41,62 @@
 namespace {
 
 constexpr int kCpMax = DCP_LSE_REDUCE_CP_MAX;
-constexpr int kWarps = 4;             // warps per CTA
-constexpr int kThreads = kWarps * 32;
+constexpr int kMaxThreads = 128;      // CTAs of 2 or 4 warps, chosen per launch
 constexpr int kVpl = 2;               // 16-byte vectors per lane per pass (64 chunks = 512 bf16)
 constexpr int kChunksPerPass = 32 * kVpl;
+constexpr int kMaxUnitsPerLaunch = 1 << 30;  // larger batches run as several launches
 
+// Kernel parameters, sized for at most kMaxCp sources. The scalars a warp needs
+// before its first load come first.
+template <int kMaxCp>
 struct Params {
-    const uint8_t* src[kCpMax];
-    const float* lse[kCpMax];
-    uint8_t* dst[kCpMax];
-    float* lse_out[kCpMax];
-    int64_t src_row, src_head;   // elements
-    int64_t lse_row, lse_head;   // elements
-    int64_t dst_row, dst_head;   // elements
-    int64_t lse_out_row;         // elements
-    int64_t units;               // B * H
-    int H, Hl, D, cp;
-    int base_e;
+    int units;                    // (row, head) pairs in this launch: rows * H
+    int H, Hl, cp, D;
+    int step;                     // warps in the grid = stride between a warp's units
+    int step_b, step_r, step_i;   // step = step_b*H + step_r*Hl + step_i, step_r < cp, step_i < Hl
+    float lse_scale;              // turns LSE differences into log2 units: 1 or log2(e)
+    float log_scale;              // turns log2(sum) into the LSE base: 1 or ln(2)
+    int64_t lse_row, lse_head;    // elements
+    int64_t src_row, src_head;    // elements
+    int64_t dst_row, dst_head;    // elements
+    int64_t lse_out_row;          // elements
+    const float* lse[kMaxCp];
+    const uint8_t* src[kMaxCp];
+    uint8_t* dst[kMaxCp];
+    float* lse_out[kMaxCp];
 };
+
+// Position of a unit: row b, destination r, local head i (global head r*Hl + i).
+struct Pos {
+    int b, r, i;
+};
+
+template <int kMaxCp>
+__device__ __forceinline__ Pos unit_pos(const Params<kMaxCp>& p, int u) {
+    Pos q;
+    q.b = (int)((unsigned)u / (unsigned)p.H);
+    const int h = u - q.b * p.H;
+    q.r = (int)((unsigned)h / (unsigned)p.Hl);
+    q.i = h - q.r * p.Hl;
+    return q;
+}
+
+// The unit `step` further on, by carries instead of divisions.
+template <int kMaxCp>
+__device__ __forceinline__ Pos advance(const Params<kMaxCp>& p, Pos q) {
+    q.b += p.step_b;
+    q.r += p.step_r;
+    q.i += p.step_i;
+    if (q.i >= p.Hl) {
+        q.i -= p.Hl;
+        q.r += 1;
+    }
+    if (q.r >= p.cp) {
+        q.r -= p.cp;
+        q.b += 1;
+    }
+    return q;
+}
 
 // ---- PTX helpers -------------------------------------------------------------
 
@@ -113,18 +151,18 @@ __device__ __forceinline__ uint32_t narrow2(float lo, float hi) {
 // ---- per-unit pieces -------------------------------------------------------
 
 template <int kMaxCp>
-__device__ __forceinline__ void load_lses(const Params& p, int64_t u, float (&l)[kMaxCp]) {
-    const int64_t b = u / p.H;
-    const int64_t h = u - b * p.H;
-    const int64_t off = b * p.lse_row + h * p.lse_head;
+__device__ __forceinline__ void load_lses(const Params<kMaxCp>& p, const Pos& q, float (&l)[kMaxCp]) {
+    const int64_t off = (int64_t)q.b * p.lse_row + (int64_t)(q.r * p.Hl + q.i) * p.lse_head;
 #pragma unroll
     for (int j = 0; j < kMaxCp; ++j) l[j] = (j < p.cp) ? ld_nc_f32(p.lse[j] + off) : -INFINITY;
 }
 
-// w_j = base^(l_j - m) / sum_k base^(l_k - m); merged = m + log_base(sum).
-// A row whose every source is -inf gets all-zero weights and merged = -inf.
+// w_j = 2^((l_j - m)*s) / sum_k 2^((l_k - m)*s), s = 1 for base-2 LSEs and
+// log2(e) for natural ones; merged = m + log2(sum) * (1 or ln 2). A row whose
+// every source is -inf gets all-zero weights and merged = -inf.
 template <int kMaxCp>
-__device__ __forceinline__ float lse_weights(const float (&l)[kMaxCp], int base_e, float (&w)[kMaxCp]) {
+__device__ __forceinline__ float lse_weights(const Params<kMaxCp>& p, const float (&l)[kMaxCp],
+                                             float (&w)[kMaxCp]) {
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kMaxCp; ++j) m = fmaxf(m, l[j]);
@@ -136,20 +174,21 @@ __device__ __forceinline__ float lse_weights(const float (&l)[kMaxCp], int base_
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxCp; ++j) {
-        const float e = (l[j] == -INFINITY) ? 0.f : (base_e ? expf(l[j] - m) : exp2f(l[j] - m));
+        const float e = (l[j] == -INFINITY) ? 0.f : exp2f((l[j] - m) * p.lse_scale);
         w[j] = e;
         s += e;
     }
+    const float inv = __frcp_rn(s);
 #pragma unroll
-    for (int j = 0; j < kMaxCp; ++j) w[j] = w[j] / s;
-    return m + (base_e ? logf(s) : log2f(s));
+    for (int j = 0; j < kMaxCp; ++j) w[j] *= inv;
+    return fmaf(log2f(s), p.log_scale, m);
 }
 
 // Issue the payload loads of sources [jb*kSB, jb*kSB + kSB) for one pass.
 // kGate: skip sources whose weight is 0 (weights known); otherwise load every
 // source j < cp (weights not known yet; zero-weight payloads are dropped later).
 template <int kSB, int kMaxCp, int kFixedChunks, bool kGate>
-__device__ __forceinline__ void load_batch(const Params& p, int64_t src_off, int jb, int pass, int lane,
+__device__ __forceinline__ void load_batch(const Params<kMaxCp>& p, int64_t src_off, int jb, int pass, int lane,
                                            int nchunks, const float (&w)[kMaxCp], uint4 (&x)[kSB][kVpl]) {
 #pragma unroll
     for (int j = 0; j < kSB; ++j) {
@@ -189,18 +228,22 @@ __device__ __forceinline__ void accumulate(int jb, int cp, const float (&w)[kMax
     }
 }
 
+template <int kMaxCp>
+__device__ __forceinline__ int64_t src_offset(const Params<kMaxCp>& p, const Pos& q) {
+    return ((int64_t)q.b * p.src_row + (int64_t)(q.r * p.Hl + q.i) * p.src_head) * 2;  // bytes
+}
+
 // ---- the kernel ----------------------------------------------------------------
 
 template <bool kF16, int kMaxCp, int kFixedChunks, bool kPreload>
-__global__ void __launch_bounds__(kThreads) lse_merge_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kMaxThreads) lse_merge_kernel(const __grid_constant__ Params<kMaxCp> p) {
     constexpr int kSB = kMaxCp < 8 ? kMaxCp : 8;  // sources per load batch
     constexpr int kNB = kMaxCp / kSB;             // load batches
     static_assert(!kPreload || (kNB == 1 && kFixedChunks == kChunksPerPass),
                   "PRELOAD needs all sources in one batch and one pass");
 
     const int lane = threadIdx.x & 31;
-    const int64_t step = (int64_t)gridDim.x * kWarps;
-    int64_t u = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    int u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
 
     // Inputs may come from the previous kernel in the stream (PDL): wait for it
     // before the first load. Let the next kernel start its launch right away.
@@ -211,27 +254,22 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(const __grid_consta
     const int nchunks = kFixedChunks ? kFixedChunks : (p.D >> 3);
     const int npass = (nchunks + kChunksPerPass - 1) / kChunksPerPass;
 
+    Pos q = unit_pos(p, u);
     float l[kMaxCp];
     float w[kMaxCp];
     uint4 x[kSB][kVpl];
-    load_lses<kMaxCp>(p, u, l);
+    load_lses<kMaxCp>(p, q, l);
     if constexpr (kPreload) {
-        const int64_t b = u / p.H;
-        const int64_t h = u - b * p.H;
-        load_batch<kSB, kMaxCp, kFixedChunks, false>(p, (b * p.src_row + h * p.src_head) * 2, 0, 0, lane,
-                                                     nchunks, w, x);
+        load_batch<kSB, kMaxCp, kFixedChunks, false>(p, src_offset(p, q), 0, 0, lane, nchunks, w, x);
     }
 
     while (true) {
-        const int64_t un = u + step;
-        const int64_t b = u / p.H;
-        const int h = (int)(u - b * p.H);
-        const int r = h / p.Hl;
-        const int i = h - r * p.Hl;
-        const int64_t src_off = (b * p.src_row + (int64_t)h * p.src_head) * 2;  // bytes
-        uint8_t* const dst = p.dst[r] + (b * p.dst_row + (int64_t)i * p.dst_head) * 2;
+        const bool more = u + p.step < p.units;
+        const Pos qn = advance(p, q);
+        const int64_t src_off = src_offset(p, q);
+        uint8_t* const dst = p.dst[q.r] + ((int64_t)q.b * p.dst_row + (int64_t)q.i * p.dst_head) * 2;
 
-        const float merged = lse_weights<kMaxCp>(l, p.base_e, w);
+        const float merged = lse_weights<kMaxCp>(p, l, w);
 
         for (int pass = 0; pass < npass; ++pass) {
             float acc[kVpl][8];
@@ -244,7 +282,7 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(const __grid_consta
                 if (jb * kSB >= p.cp) break;
                 if (!kPreload) load_batch<kSB, kMaxCp, kFixedChunks, true>(p, src_off, jb, pass, lane, nchunks, w, x);
                 // the next unit's LSEs travel while this payload is in flight
-                if (pass == 0 && jb == 0 && un < p.units) load_lses<kMaxCp>(p, un, l);
+                if (pass == 0 && jb == 0 && more) load_lses<kMaxCp>(p, qn, l);
                 accumulate<kF16, kSB, kMaxCp>(jb, p.cp, w, x, acc);
             }
 #pragma unroll
@@ -260,73 +298,147 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(const __grid_consta
                 }
             }
         }
-        if (lane == 0 && p.lse_out[r] != nullptr) p.lse_out[r][b * p.lse_out_row + i] = merged;
+        if (lane == 0 && p.lse_out[q.r] != nullptr) p.lse_out[q.r][(int64_t)q.b * p.lse_out_row + q.i] = merged;
 
-        if (un >= p.units) break;
-        u = un;
+        if (!more) break;
+        u += p.step;
+        q = qn;
         if constexpr (kPreload) {
-            const int64_t bn = u / p.H;
-            const int64_t hn = u - bn * p.H;
-            load_batch<kSB, kMaxCp, kFixedChunks, false>(p, (bn * p.src_row + hn * p.src_head) * 2, 0, 0, lane,
-                                                         nchunks, w, x);
+            load_batch<kSB, kMaxCp, kFixedChunks, false>(p, src_offset(p, q), 0, 0, lane, nchunks, w, x);
         }
     }
 }
 
 // ---- host side -----------------------------------------------------------------
 
-using KernelFn = void (*)(Params);
-
-template <bool kF16, int kMaxCp, int kFixedChunks, bool kPreload>
-KernelFn kernel_ptr() {
-    return reinterpret_cast<KernelFn>(&lse_merge_kernel<kF16, kMaxCp, kFixedChunks, kPreload>);
-}
-
-// Resident CTAs per SM for one instantiation, from the occupancy calculator
-// (queried once per instantiation; the value depends only on the kernel).
-template <bool kF16, int kMaxCp, int kFixedChunks, bool kPreload>
-int ctas_per_sm() {
-    static int cached = [] {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &n, lse_merge_kernel<kF16, kMaxCp, kFixedChunks, kPreload>, kThreads, 0) != cudaSuccess || n < 1) {
-            (void)cudaGetLastError();
-            n = 1;
-        }
-        return n;
-    }();
-    return cached;
-}
-
-struct Choice {
-    KernelFn fn;
-    int occupancy;
+// Everything a launch needs, independent of the source count.
+struct Launch {
+    const void* const* src;
+    const float* const* lse;
+    void* const* dst;
+    float* const* lse_out;
+    int cp, H, D;
+    int64_t B;
+    bool base_e, f16, fixed512;
+    dcp_lse_reduce_layout lay;
+    unsigned flags;
+    cudaStream_t stream;
+    int sms;
 };
 
+// Resident CTAs per SM for one instantiation and CTA size, from the occupancy
+// calculator (queried once; the value depends only on the kernel).
+template <typename K>
+int ctas_per_sm(K kernel, int threads, int (&cache)[2]) {
+    int& slot = cache[threads == 64 ? 0 : 1];
+    int n = __atomic_load_n(&slot, __ATOMIC_RELAXED);
+    if (n > 0) return n;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = 1;
+    }
+    __atomic_store_n(&slot, n, __ATOMIC_RELAXED);
+    return n;
+}
+
 template <bool kF16, int kMaxCp, int kFixedChunks, bool kPreload>
-Choice make_choice() {
-    return Choice{kernel_ptr<kF16, kMaxCp, kFixedChunks, kPreload>(),
-                  ctas_per_sm<kF16, kMaxCp, kFixedChunks, kPreload>()};
+int occupancy(int threads) {
+    static int cache[2] = {0, 0};
+    return ctas_per_sm(lse_merge_kernel<kF16, kMaxCp, kFixedChunks, kPreload>, threads, cache);
+}
+
+template <bool kF16, int kMaxCp, int kFixedChunks, bool kPreload>
+cudaError_t launch_one(const Launch& L, int64_t b0, int rows, int threads, int ctas) {
+    Params<kMaxCp> p;
+    const int H = L.H, Hl = L.H / L.cp, wpc = threads / 32;
+    p.units = rows * H;
+    p.H = H;
+    p.Hl = Hl;
+    p.cp = L.cp;
+    p.D = L.D;
+    p.step = ctas * wpc;
+    p.step_b = p.step / H;
+    const int sh = p.step % H;
+    p.step_r = sh / Hl;
+    p.step_i = sh % Hl;
+    p.lse_scale = L.base_e ? 1.4426950408889634f : 1.0f;
+    p.log_scale = L.base_e ? 0.6931471805599453f : 1.0f;
+    p.lse_row = L.lay.lse_row;
+    p.lse_head = L.lay.lse_head;
+    p.src_row = L.lay.src_row;
+    p.src_head = L.lay.src_head;
+    p.dst_row = L.lay.dst_row;
+    p.dst_head = L.lay.dst_head;
+    p.lse_out_row = L.lay.lse_out_row;
+    for (int j = 0; j < kMaxCp; ++j) {
+        const bool on = j < L.cp;
+        p.lse[j] = on ? L.lse[j] + b0 * L.lay.lse_row : nullptr;
+        p.src[j] = on ? static_cast<const uint8_t*>(L.src[j]) + b0 * L.lay.src_row * 2 : nullptr;
+        p.dst[j] = on ? static_cast<uint8_t*>(L.dst[j]) + b0 * L.lay.dst_row * 2 : nullptr;
+        float* lo = (on && L.lse_out != nullptr) ? L.lse_out[j] : nullptr;
+        p.lse_out[j] = lo != nullptr ? lo + b0 * L.lay.lse_out_row : nullptr;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (L.flags & DCP_FLAG_PDL) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<kF16, kMaxCp, kFixedChunks, kPreload>, p);
+}
+
+// Pick the schedule and grid for one instantiation family and launch every
+// row chunk (a chunk holds at most kMaxUnitsPerLaunch units).
+template <bool kF16, int kMaxCp, int kFixedChunks>
+cudaError_t launch_cp(const Launch& L) {
+    constexpr bool kCanPreload = (kFixedChunks == kChunksPerPass) && (kMaxCp <= 8);
+    const int64_t rows_per_launch = kMaxUnitsPerLaunch / L.H;
+    for (int64_t b0 = 0; b0 < L.B; b0 += rows_per_launch) {
+        const int rows = (int)((L.B - b0) < rows_per_launch ? (L.B - b0) : rows_per_launch);
+        const int64_t units = (int64_t)rows * L.H;
+        // One unit per warp with the payload loads issued beside the LSE loads
+        // when every warp of the grid is resident at once; otherwise one
+        // persistent wave that reads LSEs a unit ahead and skips empty sources.
+        const int wave_units = L.sms * occupancy<kF16, kMaxCp, kFixedChunks, false>(128) * 4;
+        bool preload = kCanPreload && units <= wave_units;
+        if (L.flags & DCP_FLAG_PRELOAD) preload = kCanPreload;
+        if (L.flags & DCP_FLAG_LSE_FIRST) preload = false;
+        // Small grids spread over more SMs with 2-warp CTAs; larger ones need
+        // fewer, larger CTAs.
+        const int threads = (preload && units <= 1024) ? 64 : 128;
+        const int wpc = threads / 32;
+        const int64_t want = (units + wpc - 1) / wpc;
+        cudaError_t e;
+        if constexpr (kCanPreload) {
+            if (preload) {
+                e = launch_one<kF16, kMaxCp, kFixedChunks, true>(L, b0, rows, threads, (int)want);
+                if (e != cudaSuccess) return e;
+                continue;
+            }
+        }
+        const int64_t wave = (int64_t)L.sms * occupancy<kF16, kMaxCp, kFixedChunks, false>(threads);
+        e = launch_one<kF16, kMaxCp, kFixedChunks, false>(L, b0, rows, threads, (int)(want < wave ? want : wave));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 template <bool kF16, int kMaxCp>
-Choice choose_cp(bool fixed512, bool preload) {
-    if (fixed512) {
-        if constexpr (kMaxCp <= 8) {
-            if (preload) return make_choice<kF16, kMaxCp, kChunksPerPass, true>();
-        }
-        return make_choice<kF16, kMaxCp, kChunksPerPass, false>();
-    }
-    return make_choice<kF16, kMaxCp, 0, false>();
+cudaError_t launch_d(const Launch& L) {
+    return L.fixed512 ? launch_cp<kF16, kMaxCp, kChunksPerPass>(L) : launch_cp<kF16, kMaxCp, 0>(L);
 }
 
 template <bool kF16>
-Choice choose(int cp, bool fixed512, bool preload) {
-    if (cp <= 1) return choose_cp<kF16, 1>(fixed512, preload);
-    if (cp <= 2) return choose_cp<kF16, 2>(fixed512, preload);
-    if (cp <= 4) return choose_cp<kF16, 4>(fixed512, preload);
-    if (cp <= 8) return choose_cp<kF16, 8>(fixed512, preload);
-    return choose_cp<kF16, 16>(fixed512, preload);
+cudaError_t launch_dtype(const Launch& L) {
+    if (L.cp <= 1) return launch_d<kF16, 1>(L);
+    if (L.cp <= 2) return launch_d<kF16, 2>(L);
+    if (L.cp <= 4) return launch_d<kF16, 4>(L);
+    if (L.cp <= 8) return launch_d<kF16, 8>(L);
+    return launch_d<kF16, 16>(L);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -364,39 +476,14 @@ extern "C" int dcp_lse_reduce_ex(const void* const* src_ptrs, const float* const
         return DCP_ERR_BAD_STRIDE;
     if (lay.src_row % 8 || lay.src_head % 8 || lay.dst_row % 8 || lay.dst_head % 8) return DCP_ERR_BAD_STRIDE;
 
-    Params p;
-    for (int j = 0; j < kCpMax; ++j) {
-        p.src[j] = nullptr;
-        p.lse[j] = nullptr;
-        p.dst[j] = nullptr;
-        p.lse_out[j] = nullptr;
-    }
     for (int j = 0; j < cp; ++j) {
         if (src_ptrs[j] == nullptr || lse_ptrs[j] == nullptr || dst_ptrs[j] == nullptr) return DCP_ERR_NULL_POINTER;
         if (!aligned(src_ptrs[j], 16) || !aligned(dst_ptrs[j], 16) || !aligned(lse_ptrs[j], 4))
             return DCP_ERR_MISALIGNED;
         if (lse_out_ptrs != nullptr && lse_out_ptrs[j] != nullptr && !aligned(lse_out_ptrs[j], 4))
             return DCP_ERR_MISALIGNED;
-        p.src[j] = static_cast<const uint8_t*>(src_ptrs[j]);
-        p.lse[j] = lse_ptrs[j];
-        p.dst[j] = static_cast<uint8_t*>(dst_ptrs[j]);
-        p.lse_out[j] = lse_out_ptrs != nullptr ? lse_out_ptrs[j] : nullptr;
     }
     if (B == 0) return DCP_OK;
-
-    p.src_row = lay.src_row;
-    p.src_head = lay.src_head;
-    p.lse_row = lay.lse_row;
-    p.lse_head = lay.lse_head;
-    p.dst_row = lay.dst_row;
-    p.dst_head = lay.dst_head;
-    p.lse_out_row = lay.lse_out_row;
-    p.units = B * (int64_t)H;
-    p.H = H;
-    p.Hl = Hl;
-    p.D = D;
-    p.cp = cp;
-    p.base_e = lse_base_e;
 
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
@@ -404,40 +491,23 @@ extern "C" int dcp_lse_reduce_ex(const void* const* src_ptrs, const float* const
         (void)cudaGetLastError();
         return DCP_ERR_DEVICE;
     }
-
-    const bool fixed512 = (D == 512);
-    const bool f16 = (dtype == DCP_DTYPE_F16);
-    // The PRELOAD schedule needs every source in one load batch and D = 512.
-    const bool preload_ok = fixed512 && cp <= 8;
-    // Probe the persistent schedule's occupancy to size both grids.
-    const Choice persistent = f16 ? choose<true>(cp, fixed512, false) : choose<false>(cp, fixed512, false);
-    const int64_t wave_units = (int64_t)sms * persistent.occupancy * kWarps;
-    bool preload;
-    if (flags & DCP_FLAG_PRELOAD) {
-        preload = preload_ok;
-    } else if (flags & DCP_FLAG_LSE_FIRST) {
-        preload = false;
-    } else {
-        preload = preload_ok && p.units <= wave_units;
-    }
-    const Choice c = preload ? (f16 ? choose<true>(cp, fixed512, true) : choose<false>(cp, fixed512, true))
-                             : persistent;
-    const int64_t want_ctas = (p.units + kWarps - 1) / kWarps;
-    const int64_t wave_ctas = (int64_t)sms * c.occupancy;
-    const int64_t ctas = preload ? want_ctas : (want_ctas < wave_ctas ? want_ctas : wave_ctas);
-    const unsigned grid = (unsigned)(ctas < 0x7fffffff ? ctas : 0x7fffffff);
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = (flags & DCP_FLAG_PDL) ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, c.fn, p);
+    Launch L;
+    L.src = src_ptrs;
+    L.lse = lse_ptrs;
+    L.dst = dst_ptrs;
+    L.lse_out = lse_out_ptrs;
+    L.cp = cp;
+    L.H = H;
+    L.D = D;
+    L.B = B;
+    L.base_e = lse_base_e != 0;
+    L.f16 = dtype == DCP_DTYPE_F16;
+    L.fixed512 = D == 512;
+    L.lay = lay;
+    L.flags = flags;
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.sms = sms;
+    const cudaError_t e = L.f16 ? launch_dtype<true>(L) : launch_dtype<false>(L);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return (int)e;
