@@ -124,6 +124,25 @@ __device__ __forceinline__ void st_v4(uint8_t* ptr, const uint4& v) {
                  : "memory");
 }
 
+// Hardware (MUFU) base-2 exponential, logarithm and reciprocal, each within
+// ~2 ulp; subnormal results flush to zero, so a weight below 2^-126 of the
+// largest one counts as zero.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- 16-bit <-> fp32 -----------------------------------------------------------
 
 template <bool kF16>
@@ -163,9 +182,14 @@ __device__ __forceinline__ void load_lses(const Params<kMaxCp>& p, const Pos& q,
 template <int kMaxCp>
 __device__ __forceinline__ float lse_weights(const Params<kMaxCp>& p, const float (&l)[kMaxCp],
                                              float (&w)[kMaxCp]) {
-    float m = -INFINITY;
+    float mx[kMaxCp];
 #pragma unroll
-    for (int j = 0; j < kMaxCp; ++j) m = fmaxf(m, l[j]);
+    for (int j = 0; j < kMaxCp; ++j) mx[j] = l[j];
+#pragma unroll
+    for (int half = kMaxCp / 2; half >= 1; half /= 2)
+#pragma unroll
+        for (int j = 0; j < half; ++j) mx[j] = fmaxf(mx[j], mx[j + half]);
+    const float m = mx[0];
     if (m == -INFINITY) {
 #pragma unroll
         for (int j = 0; j < kMaxCp; ++j) w[j] = 0.f;
@@ -174,14 +198,14 @@ __device__ __forceinline__ float lse_weights(const Params<kMaxCp>& p, const floa
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxCp; ++j) {
-        const float e = (l[j] == -INFINITY) ? 0.f : exp2f((l[j] - m) * p.lse_scale);
+        const float e = (l[j] == -INFINITY) ? 0.f : ex2_approx((l[j] - m) * p.lse_scale);
         w[j] = e;
         s += e;
     }
-    const float inv = __frcp_rn(s);
+    const float inv = rcp_approx(s);  // s is in [1, cp]
 #pragma unroll
     for (int j = 0; j < kMaxCp; ++j) w[j] *= inv;
-    return fmaf(log2f(s), p.log_scale, m);
+    return fmaf(lg2_approx(s), p.log_scale, m);
 }
 
 // Issue the payload loads of sources [jb*kSB, jb*kSB + kSB) for one pass.
@@ -235,8 +259,16 @@ __device__ __forceinline__ int64_t src_offset(const Params<kMaxCp>& p, const Pos
 
 // ---- the kernel ----------------------------------------------------------------
 
+// Register budget: keep 7 CTAs of 4 warps resident per SM for up to 4 sources
+// (the 512-wide PRELOAD grid of a 64-head, 64-row call then fits in one wave).
+template <int kMaxCp, int kFixedChunks>
+constexpr int min_ctas_per_sm() {
+    return (kMaxCp <= 4 && kFixedChunks == kChunksPerPass) ? 7 : 1;
+}
+
 template <bool kF16, int kMaxCp, int kFixedChunks, bool kPreload>
-__global__ void __launch_bounds__(kMaxThreads) lse_merge_kernel(const __grid_constant__ Params<kMaxCp> p) {
+__global__ void __launch_bounds__(kMaxThreads, min_ctas_per_sm<kMaxCp, kFixedChunks>())
+    lse_merge_kernel(const __grid_constant__ Params<kMaxCp> p) {
     constexpr int kSB = kMaxCp < 8 ? kMaxCp : 8;  // sources per load batch
     constexpr int kNB = kMaxCp / kSB;             // load batches
     static_assert(!kPreload || (kNB == 1 && kFixedChunks == kChunksPerPass),
@@ -244,23 +276,50 @@ __global__ void __launch_bounds__(kMaxThreads) lse_merge_kernel(const __grid_con
 
     const int lane = threadIdx.x & 31;
     int u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (u >= p.units) return;  // an exited CTA counts as having released its dependents
 
-    // Inputs may come from the previous kernel in the stream (PDL): wait for it
-    // before the first load. Let the next kernel start its launch right away.
-    pdl_wait();
-    pdl_launch_dependents();
-    if (u >= p.units) return;
-
+    // Index and address arithmetic reads only the parameters, so it runs before
+    // the wait and overlaps the previous kernel's tail under PDL: the first
+    // unit's LSE and payload addresses are pinned in registers here.
     const int nchunks = kFixedChunks ? kFixedChunks : (p.D >> 3);
     const int npass = (nchunks + kChunksPerPass - 1) / kChunksPerPass;
-
     Pos q = unit_pos(p, u);
+    const float* lp[kMaxCp];
+    const uint8_t* sp[kSB];
+    {
+        const int64_t loff = (int64_t)q.b * p.lse_row + (int64_t)(q.r * p.Hl + q.i) * p.lse_head;
+        const int64_t soff = src_offset(p, q) + (int64_t)lane * 16;
+#pragma unroll
+        for (int j = 0; j < kMaxCp; ++j) {
+            lp[j] = p.lse[j] + loff;
+            asm volatile("" : "+l"(lp[j]));
+        }
+#pragma unroll
+        for (int j = 0; j < kSB; ++j) {
+            sp[j] = p.src[j] + soff;
+            asm volatile("" : "+l"(sp[j]));
+        }
+    }
+
+    // Inputs may come from the previous kernel in the stream (PDL): wait for it
+    // before the first load. Then let the next kernel start its launch.
+    pdl_wait();
+    pdl_launch_dependents();
+
     float l[kMaxCp];
     float w[kMaxCp];
     uint4 x[kSB][kVpl];
-    load_lses<kMaxCp>(p, q, l);
+#pragma unroll
+    for (int j = 0; j < kMaxCp; ++j) l[j] = (j < p.cp) ? ld_nc_f32(lp[j]) : -INFINITY;
     if constexpr (kPreload) {
-        load_batch<kSB, kMaxCp, kFixedChunks, false>(p, src_offset(p, q), 0, 0, lane, nchunks, w, x);
+        // one pass of 64 chunks: lane's chunks are lane and 32 + lane
+#pragma unroll
+        for (int j = 0; j < kSB; ++j) {
+#pragma unroll
+            for (int v = 0; v < kVpl; ++v) {
+                x[j][v] = (j < p.cp) ? ld_stream_v4(sp[j] + v * 512) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
     }
 
     while (true) {
@@ -403,8 +462,11 @@ cudaError_t launch_cp(const Launch& L) {
         // One unit per warp with the payload loads issued beside the LSE loads
         // when every warp of the grid is resident at once; otherwise one
         // persistent wave that reads LSEs a unit ahead and skips empty sources.
-        const int wave_units = L.sms * occupancy<kF16, kMaxCp, kFixedChunks, false>(128) * 4;
-        bool preload = kCanPreload && units <= wave_units;
+        bool preload = false;
+        if constexpr (kCanPreload) {
+            const int threads = units <= 1024 ? 64 : 128;
+            preload = units <= (int64_t)L.sms * occupancy<kF16, kMaxCp, kFixedChunks, true>(threads) * (threads / 32);
+        }
         if (L.flags & DCP_FLAG_PRELOAD) preload = kCanPreload;
         if (L.flags & DCP_FLAG_LSE_FIRST) preload = false;
         // Small grids spread over more SMs with 2-warp CTAs; larger ones need
