@@ -33,7 +33,7 @@ def algorithmic_bytes(cp: int, B: int, H: int, D: int, elem: int = 2, skipped_pa
 
 
 def merge(srcs, lses, lse_base_e: bool, *, outs=None, lse_outs=None, flags: int = 0, stream=None,
-          write_lse: bool = True):
+          write_lse: bool = True, seq_lens=None, interleave: int = 1):
     """Merge cp partial outputs with the CUDA kernel.
 
     srcs: cp CUDA tensors [B, H, D] (bf16 or fp16; unit stride along D, other
@@ -41,7 +41,9 @@ def merge(srcs, lses, lse_base_e: bool, *, outs=None, lse_outs=None, flags: int 
         [B, H, 1] (any strides). Returns (outs, lse_outs): cp tensors
         [B, H/cp, D] of the sources' dtype and cp fp32 tensors [B, H/cp]
         (None entries when write_lse is False). Preallocated outs/lse_outs may
-        be passed (unit stride along D).
+        be passed (unit stride along D). seq_lens: optional CUDA int32 [B]
+        context lengths; shards owning no token of a row's context (KV
+        interleaved in blocks of ``interleave`` tokens) are masked out.
     """
     import torch
 
@@ -77,6 +79,10 @@ def merge(srcs, lses, lse_base_e: bool, *, outs=None, lse_outs=None, flags: int 
     layout = Layout(src_row=s0.stride(0), src_head=s0.stride(1), lse_row=l0.stride(0), lse_head=l0.stride(1),
                     dst_row=o0.stride(0), dst_head=o0.stride(1),
                     lse_out_row=(lo.stride(0) if lo is not None else Hl))
+    if seq_lens is not None and (seq_lens.dtype != torch.int32 or seq_lens.shape != (B,) or not seq_lens.is_cuda
+                                 or not seq_lens.is_contiguous()):
+        raise ValueError("seq_lens must be a contiguous CUDA int32 tensor of shape [B]")
     dcp_lse_reduce_ex(srcs, lses, cp, B, H, D, lse_base_e, dtype, outs,
-                      [l if l is not None else 0 for l in lse_outs], layout=layout, flags=flags, stream=stream)
+                      [l if l is not None else 0 for l in lse_outs], layout=layout, flags=flags, stream=stream,
+                      seq_lens=seq_lens, interleave=interleave)
     return outs, lse_outs

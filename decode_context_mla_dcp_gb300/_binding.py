@@ -23,6 +23,7 @@ DCP_FLAG_PRELOAD = 2
 DCP_FLAG_LSE_FIRST = 4
 
 EXPORTED_SYMBOLS = ("dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dcp_lse_reduce_version")
+DCP_LSE_REDUCE_INTERLEAVE_MAX = 1 << 24
 
 
 class DcpError(RuntimeError):
@@ -65,7 +66,7 @@ def load(path: str | None = None):
         lib.dcp_lse_reduce.restype = ci
         lib.dcp_lse_reduce_ex.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ci, i64, ci, ci, ci, ci,
                                           ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(Layout),
-                                          ctypes.c_uint, vp]
+                                          vp, ci, ctypes.c_uint, vp]
         lib.dcp_lse_reduce_ex.restype = ci
         lib.dcp_lse_reduce_strerror.argtypes = [ci]
         lib.dcp_lse_reduce_strerror.restype = ctypes.c_char_p
@@ -120,16 +121,18 @@ def dcp_lse_reduce(src_ptrs, lse_ptrs, lse_stride: int, cp: int, B: int, H: int,
 
 def dcp_lse_reduce_ex(src_ptrs, lse_ptrs, cp: int, B: int, H: int, D: int, lse_base_e: bool,
                       dtype: int, dst_ptrs, lse_out_ptrs=None, layout: Layout | dict | None = None,
-                      flags: int = 0, stream=None) -> None:
-    """The merge with explicit strides, dtype and launch flags (see the C header)."""
+                      flags: int = 0, stream=None, seq_lens=None, interleave: int = 1) -> None:
+    """The merge with explicit strides, dtype, empty-shard masking from
+    per-row context lengths (``seq_lens``: device int32 [B], KV interleaved
+    in blocks of ``interleave`` tokens) and launch flags (see the C header)."""
     lib = load()
     if isinstance(layout, dict):
         layout = Layout(**layout)
     _check(lib.dcp_lse_reduce_ex(_ptr_array(src_ptrs, cp), _ptr_array(lse_ptrs, cp), int(cp), int(B), int(H),
                                  int(D), 1 if lse_base_e else 0, int(dtype), _ptr_array(dst_ptrs, cp),
                                  _ptr_array(lse_out_ptrs, cp, allow_none=True),
-                                 ctypes.byref(layout) if layout is not None else None, int(flags),
-                                 _stream(stream)))
+                                 ctypes.byref(layout) if layout is not None else None, _ptr(seq_lens),
+                                 int(interleave), int(flags), _stream(stream)))
 
 
 def dcp_lse_reduce_strerror(status: int) -> str:

@@ -56,6 +56,8 @@ struct Params {
     int step_b, step_r, step_i;   // step = step_b*H + step_r*Hl + step_i, step_r < cp, step_i < Hl
     float lse_scale;              // turns LSE differences into log2 units: 1 or log2(e)
     float log_scale;              // turns log2(sum) into the LSE base: 1 or ln(2)
+    int interleave;               // KV tokens per interleave block (with seq_lens)
+    const int* seq_lens;          // per-row context length, or null: no masking
     int64_t lse_row, lse_head;    // elements
     int64_t src_row, src_head;    // elements
     int64_t dst_row, dst_head;    // elements
@@ -118,6 +120,12 @@ __device__ __forceinline__ float ld_nc_f32(const float* ptr) {
     return v;
 }
 
+__device__ __forceinline__ int ld_nc_s32(const int* ptr) {
+    int v;
+    asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(ptr));
+    return v;
+}
+
 __device__ __forceinline__ void st_v4(uint8_t* ptr, const uint4& v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
                  :: "l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -169,11 +177,27 @@ __device__ __forceinline__ uint32_t narrow2(float lo, float hi) {
 
 // ---- per-unit pieces -------------------------------------------------------
 
+constexpr int kNoMask = 0x7fffffff;
+
+// The unit's LSEs, and its row's context length when masking (else kNoMask).
 template <int kMaxCp>
-__device__ __forceinline__ void load_lses(const Params<kMaxCp>& p, const Pos& q, float (&l)[kMaxCp]) {
+__device__ __forceinline__ int load_lses(const Params<kMaxCp>& p, const Pos& q, float (&l)[kMaxCp]) {
     const int64_t off = (int64_t)q.b * p.lse_row + (int64_t)(q.r * p.Hl + q.i) * p.lse_head;
+    const int seq = p.seq_lens != nullptr ? ld_nc_s32(p.seq_lens + q.b) : kNoMask;
 #pragma unroll
     for (int j = 0; j < kMaxCp; ++j) l[j] = (j < p.cp) ? ld_nc_f32(p.lse[j] + off) : -INFINITY;
+    return seq;
+}
+
+// With the KV interleaved over the shards in blocks of `interleave` tokens,
+// shard j's first token is j*interleave: it owns a token of a context of `seq`
+// tokens iff seq > j*interleave. An empty shard's LSE entry is ignored.
+template <int kMaxCp>
+__device__ __forceinline__ void mask_empty(const Params<kMaxCp>& p, int seq, float (&l)[kMaxCp]) {
+    if (seq == kNoMask) return;
+#pragma unroll
+    for (int j = 0; j < kMaxCp; ++j)
+        if ((int64_t)j * p.interleave >= (int64_t)seq) l[j] = -INFINITY;
 }
 
 // w_j = 2^((l_j - m)*s) / sum_k 2^((l_k - m)*s), s = 1 for base-2 LSEs and
@@ -259,11 +283,13 @@ __device__ __forceinline__ int64_t src_offset(const Params<kMaxCp>& p, const Pos
 
 // ---- the kernel ----------------------------------------------------------------
 
-// Register budget: keep 7 CTAs of 4 warps resident per SM for up to 4 sources
-// (the 512-wide PRELOAD grid of a 64-head, 64-row call then fits in one wave).
+// Register budget for D = 512: keep 7 CTAs of 4 warps resident per SM for up
+// to 4 sources (the PRELOAD grid of a 64-head, 64-row call then fits in one
+// wave) and 4 CTAs (128 registers) for up to 8 sources.
 template <int kMaxCp, int kFixedChunks>
 constexpr int min_ctas_per_sm() {
-    return (kMaxCp <= 4 && kFixedChunks == kChunksPerPass) ? 7 : 1;
+    if (kFixedChunks != kChunksPerPass) return 1;
+    return kMaxCp <= 4 ? 7 : (kMaxCp <= 8 ? 4 : 1);
 }
 
 template <bool kF16, int kMaxCp, int kFixedChunks, bool kPreload>
@@ -286,6 +312,7 @@ __global__ void __launch_bounds__(kMaxThreads, min_ctas_per_sm<kMaxCp, kFixedChu
     Pos q = unit_pos(p, u);
     const float* lp[kMaxCp];
     const uint8_t* sp[kSB];
+    const int* slp = p.seq_lens != nullptr ? p.seq_lens + q.b : nullptr;
     {
         const int64_t loff = (int64_t)q.b * p.lse_row + (int64_t)(q.r * p.Hl + q.i) * p.lse_head;
         const int64_t soff = src_offset(p, q) + (int64_t)lane * 16;
@@ -309,6 +336,7 @@ __global__ void __launch_bounds__(kMaxThreads, min_ctas_per_sm<kMaxCp, kFixedChu
     float l[kMaxCp];
     float w[kMaxCp];
     uint4 x[kSB][kVpl];
+    int seq = slp != nullptr ? ld_nc_s32(slp) : kNoMask;
 #pragma unroll
     for (int j = 0; j < kMaxCp; ++j) l[j] = (j < p.cp) ? ld_nc_f32(lp[j]) : -INFINITY;
     if constexpr (kPreload) {
@@ -328,6 +356,7 @@ __global__ void __launch_bounds__(kMaxThreads, min_ctas_per_sm<kMaxCp, kFixedChu
         const int64_t src_off = src_offset(p, q);
         uint8_t* const dst = p.dst[q.r] + ((int64_t)q.b * p.dst_row + (int64_t)q.i * p.dst_head) * 2;
 
+        mask_empty<kMaxCp>(p, seq, l);
         const float merged = lse_weights<kMaxCp>(p, l, w);
 
         for (int pass = 0; pass < npass; ++pass) {
@@ -341,7 +370,7 @@ __global__ void __launch_bounds__(kMaxThreads, min_ctas_per_sm<kMaxCp, kFixedChu
                 if (jb * kSB >= p.cp) break;
                 if (!kPreload) load_batch<kSB, kMaxCp, kFixedChunks, true>(p, src_off, jb, pass, lane, nchunks, w, x);
                 // the next unit's LSEs travel while this payload is in flight
-                if (pass == 0 && jb == 0 && more) load_lses<kMaxCp>(p, qn, l);
+                if (pass == 0 && jb == 0 && more) seq = load_lses<kMaxCp>(p, qn, l);
                 accumulate<kF16, kSB, kMaxCp>(jb, p.cp, w, x, acc);
             }
 #pragma unroll
@@ -380,6 +409,8 @@ struct Launch {
     int64_t B;
     bool base_e, f16, fixed512;
     dcp_lse_reduce_layout lay;
+    const int32_t* seq_lens;
+    int interleave;
     unsigned flags;
     cudaStream_t stream;
     int sms;
@@ -422,6 +453,8 @@ cudaError_t launch_one(const Launch& L, int64_t b0, int rows, int threads, int c
     p.step_i = sh % Hl;
     p.lse_scale = L.base_e ? 1.4426950408889634f : 1.0f;
     p.log_scale = L.base_e ? 0.6931471805599453f : 1.0f;
+    p.interleave = L.interleave;
+    p.seq_lens = L.seq_lens != nullptr ? L.seq_lens + b0 : nullptr;
     p.lse_row = L.lay.lse_row;
     p.lse_head = L.lay.lse_head;
     p.src_row = L.lay.src_row;
@@ -510,7 +543,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 extern "C" int dcp_lse_reduce_ex(const void* const* src_ptrs, const float* const* lse_ptrs,
                                  int cp, int64_t B, int H, int D, int lse_base_e, int dtype,
                                  void* const* dst_ptrs, float* const* lse_out_ptrs,
-                                 const dcp_lse_reduce_layout* layout, unsigned flags, void* stream) {
+                                 const dcp_lse_reduce_layout* layout, const int32_t* seq_lens, int interleave,
+                                 unsigned flags, void* stream) {
     if (src_ptrs == nullptr || lse_ptrs == nullptr || dst_ptrs == nullptr) return DCP_ERR_NULL_POINTER;
     if (cp < 1 || cp > kCpMax) return DCP_ERR_BAD_CP;
     if (B < 0 || H < 1 || D < 8 || D % 8 != 0) return DCP_ERR_BAD_SHAPE;
@@ -519,6 +553,10 @@ extern "C" int dcp_lse_reduce_ex(const void* const* src_ptrs, const float* const
     if (lse_base_e != 0 && lse_base_e != 1) return DCP_ERR_BAD_BASE;
     if ((flags & ~(DCP_FLAG_PDL | DCP_FLAG_PRELOAD | DCP_FLAG_LSE_FIRST)) != 0) return DCP_ERR_BAD_FLAGS;
     if ((flags & DCP_FLAG_PRELOAD) && (flags & DCP_FLAG_LSE_FIRST)) return DCP_ERR_BAD_FLAGS;
+    if (seq_lens != nullptr) {
+        if (interleave < 1 || interleave > DCP_LSE_REDUCE_INTERLEAVE_MAX) return DCP_ERR_BAD_INTERLEAVE;
+        if (!aligned(seq_lens, 4)) return DCP_ERR_MISALIGNED;
+    }
 
     const int Hl = H / cp;
     dcp_lse_reduce_layout lay;
@@ -566,6 +604,8 @@ extern "C" int dcp_lse_reduce_ex(const void* const* src_ptrs, const float* const
     L.f16 = dtype == DCP_DTYPE_F16;
     L.fixed512 = D == 512;
     L.lay = lay;
+    L.seq_lens = seq_lens;
+    L.interleave = seq_lens != nullptr ? interleave : 1;
     L.flags = flags;
     L.stream = static_cast<cudaStream_t>(stream);
     L.sms = sms;
@@ -594,7 +634,7 @@ extern "C" int dcp_lse_reduce(const void* const* src_ptrs, const float* const* l
     lay.dst_head = D;
     lay.lse_out_row = H / cp;
     return dcp_lse_reduce_ex(src_ptrs, lse_ptrs, cp, B, H, D, lse_base_e, DCP_DTYPE_BF16, dst_ptrs, lse_out_ptrs,
-                             &lay, 0u, stream);
+                             &lay, nullptr, 1, 0u, stream);
 }
 
 extern "C" const char* dcp_lse_reduce_strerror(int status) {
@@ -611,6 +651,7 @@ extern "C" const char* dcp_lse_reduce_strerror(int status) {
         case DCP_ERR_BAD_DTYPE: return "dtype must be DCP_DTYPE_BF16 or DCP_DTYPE_F16";
         case DCP_ERR_BAD_BASE: return "lse_base_e must be 0 (base 2) or 1 (base e)";
         case DCP_ERR_DEVICE: return "could not query the current CUDA device";
+        case DCP_ERR_BAD_INTERLEAVE: return "interleave must be in [1, 2^24] when seq_lens is given";
         default: break;
     }
     if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));

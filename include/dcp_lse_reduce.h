@@ -57,6 +57,7 @@ extern "C" {
 #endif
 
 #define DCP_LSE_REDUCE_CP_MAX 16
+#define DCP_LSE_REDUCE_INTERLEAVE_MAX (1 << 24)
 
 /* Element types of the partial outputs and of the merged output. */
 #define DCP_DTYPE_BF16 0
@@ -86,7 +87,8 @@ enum {
     DCP_ERR_BAD_FLAGS = -7,     /* unknown flag bits, or PRELOAD with LSE_FIRST */
     DCP_ERR_BAD_DTYPE = -8,     /* dtype not DCP_DTYPE_BF16 / DCP_DTYPE_F16 */
     DCP_ERR_BAD_BASE = -9,      /* lse_base_e not 0 or 1 */
-    DCP_ERR_DEVICE = -10        /* the current device could not be queried */
+    DCP_ERR_DEVICE = -10,       /* the current device could not be queried */
+    DCP_ERR_BAD_INTERLEAVE = -11 /* seq_lens given with interleave outside [1, 2^24] */
 };
 
 /*
@@ -135,16 +137,32 @@ typedef struct dcp_lse_reduce_layout {
 /*
  * The same merge with explicit strides (padded token strides, heads taken from
  * a wider backing array, FlashMLA-style LSE head strides), a dtype
- * (DCP_DTYPE_BF16 or DCP_DTYPE_F16; the output has the input's type) and
- * launch flags (DCP_FLAG_*). layout = NULL means contiguous buffers with
- * lse_row = H. Sources: the pages cited above, and "[Attention] Add direct
- * symmetric-memory DCP A2A" (vLLM #48897) commit notes on padded token
- * strides, non-contiguous head storage and fp16/bf16 outputs.
+ * (DCP_DTYPE_BF16 or DCP_DTYPE_F16; the output has the input's type),
+ * optional masking of empty shards from the rows' context lengths, and launch
+ * flags (DCP_FLAG_*). layout = NULL means contiguous buffers with lse_row = H.
+ *
+ *   seq_lens    NULL, or a device array of B int32 context lengths (4-byte
+ *               aligned). The KV of a row is interleaved over the cp shards in
+ *               blocks of `interleave` tokens (token t lives on shard
+ *               (t / interleave) % cp), so shard j owns a token of a context
+ *               of L tokens iff L > j*interleave. A shard that owns none is
+ *               empty for that row: its LSE entry is ignored (it may hold
+ *               anything) and its payload is neither read nor added. L = 0
+ *               gives an output of 0 and a merged LSE of -inf.
+ *   interleave  tokens per interleave block, 1..DCP_LSE_REDUCE_INTERLEAVE_MAX
+ *               (read only when seq_lens is given).
+ *
+ * Sources: the pages cited above; "[Attention] Add direct symmetric-memory DCP
+ * A2A" (vLLM #48897) commit notes on padded token strides, non-contiguous head
+ * storage, fp16/bf16 outputs, and empty-KV-shard masking from the decode
+ * seq_lens; "[DCP] Optimize shared Output, Query, and Indexer/Top-K via peer
+ * memory" (sglang #32851) commit notes on the KV interleaved across DCP ranks.
  */
 int dcp_lse_reduce_ex(const void* const* src_ptrs, const float* const* lse_ptrs,
                       int cp, int64_t B, int H, int D, int lse_base_e, int dtype,
                       void* const* dst_ptrs, float* const* lse_out_ptrs,
-                      const dcp_lse_reduce_layout* layout, unsigned flags, void* stream);
+                      const dcp_lse_reduce_layout* layout, const int32_t* seq_lens, int interleave,
+                      unsigned flags, void* stream);
 
 /* A static, human-readable message for a status code. */
 const char* dcp_lse_reduce_strerror(int status);

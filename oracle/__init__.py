@@ -66,6 +66,7 @@ def open_library(path: str):
         ctypes.c_int, ctypes.POINTER(vp), ctypes.c_int64, ctypes.c_int64,
         ctypes.c_int, ctypes.POINTER(vp), ctypes.c_int64, ctypes.c_int64,
         ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_int,
         ctypes.POINTER(vp), ctypes.POINTER(vp)]
     lib.oracle_dcp_merge.restype = ctypes.c_int
     lib.oracle_half_bits_to_double.argtypes = [ctypes.c_int, ctypes.c_uint16]
@@ -84,7 +85,7 @@ def _load():
 
 def merge(srcs, lses, lse_base_e: bool, *, dtype: str = "bf16", H: int | None = None,
           D: int | None = None, src_strides: tuple[int, int] | None = None,
-          lse_strides: tuple[int, int] | None = None):
+          lse_strides: tuple[int, int] | None = None, seq_lens=None, interleave: int = 1):
     """Merge cp partial outputs into cp destinations, in fp64.
 
     srcs: cp arrays. For dtype 'bf16'/'f16' they hold raw 16-bit patterns
@@ -93,6 +94,9 @@ def merge(srcs, lses, lse_base_e: bool, *, dtype: str = "bf16", H: int | None = 
         contiguous [B, H, D] array.
     lses: cp float32 (or float64) arrays indexed flat[b*lse_row + h*lse_head];
         the default is contiguous [B, H] (FlashMLA's [B, H, 1] is the same).
+    seq_lens: optional [B] context lengths; with the KV interleaved over the
+        shards in blocks of ``interleave`` tokens, a shard that owns no token
+        of a row's context is empty for that row (LSE ignored, weight 0).
     Returns (outs, lse_outs): cp arrays of shape [B, H/cp, D] and [B, H/cp],
     float64.
     """
@@ -135,6 +139,11 @@ def merge(srcs, lses, lse_base_e: bool, *, dtype: str = "bf16", H: int | None = 
     outs = [np.empty((B, Hl, D), dtype=np.float64) for _ in range(cp)]
     lse_outs = [np.empty((B, Hl), dtype=np.float64) for _ in range(cp)]
 
+    sl = None
+    if seq_lens is not None:
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        if sl.shape != (B,):
+            raise ValueError("seq_lens must have one entry per row")
     vp = ctypes.c_void_p
     arr = vp * cp
     lib = _load()
@@ -142,6 +151,7 @@ def merge(srcs, lses, lse_base_e: bool, *, dtype: str = "bf16", H: int | None = 
         code, arr(*[a.ctypes.data for a in src_arrays]), src_strides[0], src_strides[1],
         lse_code, arr(*[a.ctypes.data for a in lse_arrays]), lse_strides[0], lse_strides[1],
         cp, B, H, D, 1 if lse_base_e else 0,
+        sl.ctypes.data if sl is not None else None, int(interleave),
         arr(*[o.ctypes.data for o in outs]), arr(*[o.ctypes.data for o in lse_outs]))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")

@@ -80,6 +80,20 @@ static double load_lse(int lse_dtype, const void* base, int64_t idx) {
 }
 
 /*
+ * Does source (shard) j own any token of a context of `len` tokens? The KV
+ * cache is interleaved over the cp shards in blocks of `interleave` tokens:
+ * token t belongs to shard (t / interleave) % cp ("[DCP] Optimize shared
+ * Output, Query, and Indexer/Top-K via peer memory", commit notes: the latent
+ * KV stays interleaved across DCP ranks). Counted token by token.
+ */
+static int shard_owns_tokens(int64_t len, int j, int cp, int interleave) {
+    for (int64_t t = 0; t < len; ++t) {
+        if ((t / interleave) % cp == j) return 1; /* found one owned token */
+    }
+    return 0;
+}
+
+/*
  * Merge cp partial outputs for every destination r in [0, cp).
  *
  *   src[j]      source j's partial output, element (b, h, d) at
@@ -89,14 +103,23 @@ static double load_lse(int lse_dtype, const void* base, int64_t idx) {
  *               (b*(H/cp) + i)*D + d
  *   lse_out[r]  destination r's merged LSE, fp64, element (b, i) at
  *               b*(H/cp) + i; may be NULL
+ *   seq_lens    optional (NULL = no masking): context length of each row. A
+ *               source that owns no token of row b's context is empty for
+ *               that row: its LSE entry is ignored and it gets weight 0
+ *               ("[Attention] Add direct symmetric-memory DCP A2A", commit
+ *               notes: the combine masks empty-KV-shard rows given the decode
+ *               seq_lens).
+ *   interleave  tokens per interleave block (>= 1), used with seq_lens.
  *
  * Returns 0, or -1 on an argument the oracle does not take.
  */
 int oracle_dcp_merge(int dtype, const void* const* src, int64_t src_row, int64_t src_head,
                      int lse_dtype, const void* const* lse, int64_t lse_row, int64_t lse_head,
                      int cp, int64_t B, int H, int D, int lse_base_e,
+                     const int32_t* seq_lens, int interleave,
                      double* const* out, double* const* lse_out) {
     if (cp < 1 || cp > ORACLE_CP_MAX || B < 0 || H < 1 || D < 1 || H % cp != 0) return -1;
+    if (seq_lens && interleave < 1) return -1;
     if (dtype < ORACLE_BF16 || dtype > ORACLE_F64) return -1;
     if (lse_dtype != ORACLE_LSE_F32 && lse_dtype != ORACLE_LSE_F64) return -1;
     const int Hl = H / cp;
@@ -109,7 +132,11 @@ int oracle_dcp_merge(int dtype, const void* const* src, int64_t src_row, int64_t
                 double L[ORACLE_CP_MAX];
                 double m = -INFINITY;
                 for (int j = 0; j < cp; ++j) {
-                    L[j] = load_lse(lse_dtype, lse[j], b * lse_row + (int64_t)h * lse_head) * to_e;
+                    if (seq_lens && !shard_owns_tokens(seq_lens[b], j, cp, interleave)) {
+                        L[j] = -INFINITY; /* empty shard: its LSE entry is not read */
+                    } else {
+                        L[j] = load_lse(lse_dtype, lse[j], b * lse_row + (int64_t)h * lse_head) * to_e;
+                    }
                     if (L[j] > m) m = L[j];
                 }
                 double* o = out[r] + (b * Hl + i) * (int64_t)D;

@@ -87,14 +87,18 @@ def test_ex_rejects_bad_flags_dtype_strides(lib):
     p = arr(FAKE, FAKE)
     q = arr(FAKE + 4096, FAKE + 4096)
 
-    def ex(dtype=0, flags=0, layout=None, base_e=1):
+    def ex(dtype=0, flags=0, layout=None, base_e=1, seq_lens=None, interleave=1):
         return lib.dcp_lse_reduce_ex(p, p, 2, 1, 4, 512, base_e, dtype, q, None,
-                                     ctypes.byref(layout) if layout is not None else None, flags, None)
+                                     ctypes.byref(layout) if layout is not None else None, seq_lens, interleave,
+                                     flags, None)
 
     assert ex(dtype=2) == -8
     assert ex(base_e=2) == -9
     assert ex(flags=8) == -7
     assert ex(flags=dcp.DCP_FLAG_PRELOAD | dcp.DCP_FLAG_LSE_FIRST) == -7
+    assert ex(seq_lens=FAKE, interleave=0) == -11
+    assert ex(seq_lens=FAKE, interleave=(1 << 24) + 1) == -11
+    assert ex(seq_lens=FAKE + 2, interleave=1) == -6
     good = dict(src_row=2048, src_head=512, lse_row=4, lse_head=1, dst_row=1024, dst_head=512, lse_out_row=2)
     for key, bad in [("src_row", 2044), ("src_head", 4), ("dst_row", -8), ("dst_head", 12), ("lse_row", -1)]:
         lay = dcp.Layout(**{**good, key: bad})

@@ -268,6 +268,55 @@ def test_strided_layouts(oracle_mod):
         assert (dst_back[r][:, 0] == 0).all() and (dst_back[r][:, :, D:] == 0).all()
 
 
+@pytest.mark.parametrize("cfg,interleave", [("kimi", 1), ("kimi", 16), ("deepseek", 1), ("deepseek", 64)])
+@pytest.mark.parametrize("flags", [0, dcp.DCP_FLAG_PRELOAD, dcp.DCP_FLAG_LSE_FIRST])
+def test_seq_len_masking(oracle_mod, cfg, interleave, flags):
+    # Context lengths around every shard boundary (L <= j*interleave empties
+    # shard j), including 0. Empty shards' LSE entries hold NaN and their
+    # payloads NaN: both must be ignored.
+    inp = make_merge_inputs(cfg, 40, seed=interleave)
+    cp, B, H = inp.cp, inp.B, inp.H
+    rng = np.random.default_rng(interleave)
+    lens = rng.integers(0, cp * interleave + 3, size=B).astype(np.int32)
+    lens[:4] = [0, 1, interleave, cp * interleave]
+    for j in range(cp):
+        empty = lens <= j * interleave
+        inp.lses[j] = inp.lses[j].copy()
+        inp.lses[j].reshape(B, H)[empty] = np.nan
+        inp.srcs[j][empty] = BF16_QNAN
+    srcs = [to_dev_bits(s) for s in inp.srcs]
+    lses = [torch.from_numpy(l).cuda() for l in inp.lses]
+    sl = torch.from_numpy(lens).cuda()
+    outs, louts = dcp.merge(srcs, lses, inp.lse_base_e, seq_lens=sl, interleave=interleave, flags=flags)
+    torch.cuda.synchronize()
+    ref, lref = oracle_mod.merge(inp.srcs, [l.reshape(B, H) for l in inp.lses], inp.lse_base_e, seq_lens=lens,
+                                 interleave=interleave)
+    for r in range(cp):
+        assert_out_close(outs[r].float().double().cpu().numpy(), ref[r], f"masked dest {r}")
+        assert_lse_close(louts[r].double().cpu().numpy(), lref[r], f"masked dest {r}")
+    # L = 0 rows
+    for r in range(cp):
+        assert (outs[r][0] == 0).all() and (louts[r][0] == -float("inf")).all()
+
+
+def test_seq_len_masking_matches_split_attention_over_row_contexts(oracle_mod):
+    # Partials from fp64 attention over each row's interleaved shards, rounded
+    # to bf16; the masked GPU merge must reproduce attention over the row's
+    # whole context.
+    from tests.test_oracle_pins import _masked_case
+    cp, interleave, lens = 4, 4, [3, 9, 17]
+    srcs64, lses64, o_full, l_full = _masked_case(cp, interleave, lens)
+    srcs = [to_dev_bits(bf16_bits(np.nan_to_num(s, nan=0.0).astype(np.float32))) for s in srcs64]
+    lses = [torch.from_numpy(l.astype(np.float32)).cuda() for l in lses64]
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    outs, louts = dcp.merge(srcs, lses, True, seq_lens=sl, interleave=interleave)
+    torch.cuda.synchronize()
+    got = torch.cat(outs, 1).float().double().cpu().numpy()
+    assert (np.abs(got - o_full) <= ATOL + RTOL * np.abs(o_full)).all()
+    lg = torch.cat(louts, 1).double().cpu().numpy()
+    assert (np.abs(lg - l_full) <= LSE_R * np.maximum(np.abs(l_full), 1)).all()
+
+
 def test_empty_batch_writes_nothing():
     inp = make_merge_inputs("kimi", 1, seed=0)
     srcs = [to_dev_bits(s) for s in inp.srcs]

@@ -21,6 +21,9 @@ MUTANTS = {
     "zero_weight_still_read": ("if (w[j] == 0.0) continue;", ""),
     "empty_row_not_special": ("if (m == -INFINITY) {", "if (0) {"),
     "src_head_stride_ignored": ("(int64_t)h * src_head + d", "(int64_t)h * D + d"),
+    "interleave_ignored": ("if ((t / interleave) % cp == j) return 1;", "if (t % cp == j) return 1;"),
+    "seq_len_mask_ignored": ("if (seq_lens && !shard_owns_tokens", "if (0 && !shard_owns_tokens"),
+    "seq_len_off_by_one": ("for (int64_t t = 0; t < len; ++t) {", "for (int64_t t = 0; t <= len; ++t) {"),
 }
 
 # pins that take only the oracle module (and, where parametrised, fixed args)
@@ -41,6 +44,9 @@ PIN_CALLS = [
     (pins.test_padded_source_rows, {}),
     (pins.test_non_contiguous_head_storage, {}),
     (pins.test_merge_of_split_attention_is_full_attention, dict(split="halves", base_e=True)),
+    (pins.test_seq_len_mask_gives_attention_over_the_row_context, dict(cp=4, interleave=4, lens=[3, 9, 17])),
+    (pins.test_seq_len_mask_gives_attention_over_the_row_context, dict(cp=4, interleave=1, lens=[1, 2, 64])),
+    (pins.test_zero_length_context_is_an_empty_row, {}),
 ]
 
 

@@ -314,3 +314,58 @@ def test_empty_shard_in_split_attention(oracle_mod):
     outs, lse_outs = oracle_mod.merge(o_parts, l_parts, True, dtype="f64")
     np.testing.assert_allclose(concat_heads(outs), o_full, rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(np.concatenate(lse_outs, 1), l_full, rtol=1e-15)
+
+
+# --- seq_lens-driven empty-shard masking -----------------------------------------
+
+def _masked_case(cp, interleave, lens, seed=0):
+    """Partials of attention over each row's first lens[b] tokens, split over
+    cp shards with the KV interleaved in blocks of `interleave` tokens. Empty
+    shards get a NaN payload and a garbage (+7) LSE entry, which the mask must
+    ignore. Returns (partials, lses, full attention o, full lse)."""
+    from oracle.attention import attention
+    q, kv = tiny_qkv(seed=seed)
+    scale = 1.0 / math.sqrt(512)
+    R, H, D = q.shape
+    srcs = [np.empty((R, H, D)) for _ in range(cp)]
+    lses = [np.empty((R, H)) for _ in range(cp)]
+    o_full = np.empty((R, H, D))
+    l_full = np.empty((R, H))
+    for b in range(R):
+        toks = np.arange(lens[b])
+        for j in range(cp):
+            own = toks[(toks // interleave) % cp == j]
+            o, l = attention(q[b:b + 1], kv[own], scale)
+            if own.size == 0:
+                o[:] = np.nan
+                l[:] = 7.0
+            srcs[j][b], lses[j][b] = o[0], l[0]
+        o, l = attention(q[b:b + 1], kv[toks], scale)
+        o_full[b], l_full[b] = o[0], l[0]
+    return srcs, lses, o_full, l_full
+
+
+@pytest.mark.parametrize("cp,interleave,lens", [(4, 1, [1, 2, 64]), (4, 4, [3, 9, 17]), (2, 16, [5, 16, 40]),
+                                                 (8, 2, [1, 15, 16])])
+def test_seq_len_mask_gives_attention_over_the_row_context(oracle_mod, cp, interleave, lens):
+    srcs, lses, o_full, l_full = _masked_case(cp, interleave, lens)
+    outs, lse_outs = oracle_mod.merge(srcs, lses, True, dtype="f64", seq_lens=np.array(lens),
+                                      interleave=interleave)
+    np.testing.assert_allclose(concat_heads(outs), o_full, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(np.concatenate(lse_outs, 1), l_full, rtol=1e-13)
+
+
+def test_zero_length_context_is_an_empty_row(oracle_mod):
+    inp = make_merge_inputs("kimi", rows=3, seed=41, cp=4, H=8, D=16)
+    outs, lse_outs = oracle_mod.merge(inp.srcs, inp.lses, False, seq_lens=np.array([0, 5, 0]), interleave=1)
+    for r in range(4):
+        assert np.array_equal(outs[r][[0, 2]], np.zeros((2, 2, 16)))
+        assert np.all(lse_outs[r][[0, 2]] == -np.inf) and np.isfinite(lse_outs[r][1]).all()
+
+
+def test_long_contexts_mask_nothing(oracle_mod):
+    inp = make_merge_inputs("deepseek", rows=4, seed=43, cp=8, H=16, D=16)
+    a, la = oracle_mod.merge(inp.srcs, inp.lses, True)
+    b, lb = oracle_mod.merge(inp.srcs, inp.lses, True, seq_lens=np.array([64, 100, 1 << 20, 65]), interleave=8)
+    for r in range(8):
+        assert np.array_equal(a[r], b[r]) and np.array_equal(la[r], lb[r])
