@@ -97,6 +97,71 @@ def recorded_traffic():
     return d.get("per_launch_bytes_bench_step")
 
 
+class NvmlClockSampler:
+    """Read-only NVML samples (every few ms) of this GPU's SM clock, power and
+    clock-event (throttle) reasons, through the driver's libnvidia-ml."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str, period_s: float = 0.005):
+        import ctypes
+        self.ct = ctypes
+        self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nvml.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for " + uuid)
+        self.reason_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.period = period_s
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+
+    def _one(self):
+        ct = self.ct
+        c, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(c)) != 0:
+            return None
+        self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        self.nvml.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+        self.reason_fn(self.h, ct.byref(rs))
+        return c.value, mx.value, mw.value / 1000.0, rs.value
+
+    def start(self):
+        def run():
+            while not self.stop_flag.is_set():
+                v = self._one()
+                if v is not None:
+                    self.samples.append(v)
+                self.stop_flag.wait(self.period)
+        self.thread = threading.Thread(target=run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.stop_flag.set()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm = [x[0] for x in self.samples]
+        reasons = set()
+        for x in self.samples:
+            for bit, name in self.REASONS.items():
+                if x[3] & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(x[1] for x in self.samples) if sm else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(x[2] for x in self.samples) if sm else None, "source": "nvml"}
+
+
+def clock_sampler(uuid):
+    try:
+        return NvmlClockSampler(uuid)
+    except (OSError, AttributeError, TypeError):
+        return ClockSampler(uuid)
+
+
 class ClockSampler:
     """nvidia-smi samples of this GPU's clocks and throttle reasons."""
     FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -152,7 +217,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+                "power_w_max": max(power) if power else None, "source": "nvidia-smi"}
 
 
 # ---------------------------------------------------------------------------- the workload
@@ -437,9 +502,9 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(cfg.rows) + 1)] for _ in range(args.steps)]
-    sampler = ClockSampler(uuid)
+    sampler = clock_sampler(uuid)
     sampler.start()
-    time.sleep(0.3)
+    time.sleep(0.3 if isinstance(sampler, ClockSampler) else 0.02)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
