@@ -15,10 +15,12 @@ from torch tensors and allocates the outputs.
 from __future__ import annotations
 
 from ._binding import (DCP_DTYPE_BF16, DCP_DTYPE_F16, DCP_FLAG_LSE_FIRST, DCP_FLAG_PDL, DCP_FLAG_PRELOAD,
-                       DCP_LSE_REDUCE_CP_MAX, EXPORTED_SYMBOLS, DcpError, Layout, dcp_lse_reduce,
-                       dcp_lse_reduce_ex, dcp_lse_reduce_strerror, dcp_lse_reduce_version, library_path, load)
+                       DCP_LSE_REDUCE_CP_MAX, DCP_MLA_SPLIT_MAX, EXPORTED_SYMBOLS, DcpError, Layout,
+                       dcp_lse_reduce, dcp_lse_reduce_ex, dcp_lse_reduce_strerror, dcp_lse_reduce_version,
+                       dcp_mla_decode_partial, dcp_mla_decode_smem_bytes, library_path, load)
 
 __all__ = ["dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dcp_lse_reduce_version", "merge",
+           "dcp_mla_decode_partial", "dcp_mla_decode_smem_bytes", "mla_decode_partial", "DCP_MLA_SPLIT_MAX",
            "algorithmic_bytes", "Layout", "DcpError", "load", "library_path", "EXPORTED_SYMBOLS",
            "DCP_DTYPE_BF16", "DCP_DTYPE_F16", "DCP_FLAG_PDL", "DCP_FLAG_PRELOAD", "DCP_FLAG_LSE_FIRST",
            "DCP_LSE_REDUCE_CP_MAX"]
@@ -86,3 +88,29 @@ def merge(srcs, lses, lse_base_e: bool, *, outs=None, lse_outs=None, flags: int 
                       [l if l is not None else 0 for l in lse_outs], layout=layout, flags=flags, stream=stream,
                       seq_lens=seq_lens, interleave=interleave)
     return outs, lse_outs
+
+
+def mla_decode_partial(q, kv, kv_len, scale: float, *, lse_base_e: bool = True, n_split: int = 1, dv: int = 512,
+                       outs=None, lses=None, status=None, flags: int = 0, stream=None):
+    """Split-KV MLA decode attention over one shard with the CUDA kernel.
+
+    q: CUDA bf16 [B, H, Dk]; kv: CUDA bf16 [B, T, Dk] (row b's shard-local
+    tokens); kv_len: CUDA int32 [B]. Returns (outs, lses): n_split bf16
+    [B, H, dv] partial outputs and n_split fp32 [B, H] LSEs, one per contiguous
+    token range of each row.
+    """
+    import torch
+
+    B, H, Dk = q.shape
+    T = kv.shape[1]
+    if q.dtype != torch.bfloat16 or kv.dtype != torch.bfloat16 or not (q.is_contiguous() and kv.is_contiguous()):
+        raise ValueError("q and kv must be contiguous bf16 CUDA tensors")
+    if kv.shape[0] != B or kv.shape[2] != Dk or kv_len.dtype != torch.int32 or kv_len.shape != (B,):
+        raise ValueError("kv must be [B, T, Dk] and kv_len int32 [B]")
+    if outs is None:
+        outs = [torch.empty((B, H, dv), dtype=torch.bfloat16, device=q.device) for _ in range(n_split)]
+    if lses is None:
+        lses = [torch.empty((B, H), dtype=torch.float32, device=q.device) for _ in range(n_split)]
+    dcp_mla_decode_partial(q, kv, kv_len, B, H, Dk, dv, T, scale, lse_base_e, n_split, outs, lses, status=status,
+                           flags=flags, stream=stream)
+    return outs, lses

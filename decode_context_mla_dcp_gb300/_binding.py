@@ -22,7 +22,14 @@ DCP_FLAG_PDL = 1
 DCP_FLAG_PRELOAD = 2
 DCP_FLAG_LSE_FIRST = 4
 
-EXPORTED_SYMBOLS = ("dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dcp_lse_reduce_version")
+EXPORTED_SYMBOLS = ("dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dcp_lse_reduce_version",
+                    "dcp_mla_decode_partial", "dcp_mla_decode_smem_bytes")
+DCP_MLA_SPLIT_MAX = 16
+_MLA_ERRORS = {-101: "q, kv, kv_len, out_ptrs, lse_ptrs or an entry is NULL",
+               -102: "B must be in [0, 65535], T >= 0, H a positive multiple of 16, Dk 512 or 576, Dv 512",
+               -103: "n_split must be in [1, 16]",
+               -104: "q, kv and outputs must be 16-byte aligned; LSE, kv_len and status 4-byte aligned",
+               -105: "only DCP_FLAG_PDL is accepted"}
 DCP_LSE_REDUCE_INTERLEAVE_MAX = 1 << 24
 
 
@@ -72,6 +79,11 @@ def load(path: str | None = None):
         lib.dcp_lse_reduce_strerror.restype = ctypes.c_char_p
         lib.dcp_lse_reduce_version.argtypes = []
         lib.dcp_lse_reduce_version.restype = ci
+        lib.dcp_mla_decode_partial.argtypes = [vp, vp, vp, i64, ci, ci, ci, i64, ctypes.c_float, ci, ci,
+                                               ctypes.POINTER(vp), ctypes.POINTER(vp), vp, ctypes.c_uint, vp]
+        lib.dcp_mla_decode_partial.restype = ci
+        lib.dcp_mla_decode_smem_bytes.argtypes = [ci, ci]
+        lib.dcp_mla_decode_smem_bytes.restype = ci
         if path is None:
             _lib = lib
         return lib
@@ -136,7 +148,24 @@ def dcp_lse_reduce_ex(src_ptrs, lse_ptrs, cp: int, B: int, H: int, D: int, lse_b
 
 
 def dcp_lse_reduce_strerror(status: int) -> str:
+    if int(status) in _MLA_ERRORS:
+        return _MLA_ERRORS[int(status)]
     return load().dcp_lse_reduce_strerror(int(status)).decode()
+
+
+def dcp_mla_decode_partial(q, kv, kv_len, B: int, H: int, Dk: int, Dv: int, T: int, scale: float,
+                           lse_base_e: bool, n_split: int, out_ptrs, lse_ptrs, status=None, flags: int = 0,
+                           stream=None) -> None:
+    """Split-KV MLA decode attention over one shard (see include/dcp_mla_decode.h)."""
+    lib = load()
+    _check(lib.dcp_mla_decode_partial(_ptr(q), _ptr(kv), _ptr(kv_len), int(B), int(H), int(Dk), int(Dv), int(T),
+                                      float(scale), 1 if lse_base_e else 0, int(n_split),
+                                      _ptr_array(out_ptrs, n_split), _ptr_array(lse_ptrs, n_split), _ptr(status),
+                                      int(flags), _stream(stream)))
+
+
+def dcp_mla_decode_smem_bytes(Dk: int, H: int) -> int:
+    return int(load().dcp_mla_decode_smem_bytes(int(Dk), int(H)))
 
 
 def dcp_lse_reduce_version() -> int:

@@ -15,8 +15,8 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "dcp_lse_reduce.cu")]
-HEADERS = [os.path.join(ROOT, "include", "dcp_lse_reduce.h")]
+SOURCES = [os.path.join(PKG, "csrc", "dcp_lse_reduce.cu"), os.path.join(PKG, "csrc", "mla_decode_partial.cu")]
+HEADERS = [os.path.join(ROOT, "include", "dcp_lse_reduce.h"), os.path.join(ROOT, "include", "dcp_mla_decode.h")]
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libdcp_lse_reduce.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
@@ -47,11 +47,26 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not is_stale():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc_path(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-o", tmp, *SOURCES]
+    tag = f".tmp{os.getpid()}"
+    objs = [os.path.join(BUILD_DIR, os.path.basename(src) + tag + ".o") for src in SOURCES]
+    compile_flags = [f for f in NVCC_FLAGS if f != "-shared"]
+    procs = []
+    for src, obj in zip(SOURCES, objs):
+        cmd = [nvcc_path(), *compile_flags, "-I", os.path.join(ROOT, "include"), "-c", "-o", obj, src]
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        procs.append((cmd, subprocess.Popen(cmd)))
+    for cmd, pr in procs:
+        if pr.wait() != 0:
+            raise subprocess.CalledProcessError(pr.returncode, cmd)
+    tmp = LIB_PATH + tag
+    cmd = [nvcc_path(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-cudart", "static", "-o", tmp,
+           *objs]
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)
+    for obj in objs:
+        os.remove(obj)
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

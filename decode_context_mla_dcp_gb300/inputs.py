@@ -27,9 +27,13 @@ from dataclasses import dataclass, field
 import numpy as np
 
 __all__ = ["MergeConfig", "MergeInputs", "CONFIGS", "bf16_bits", "f16_bits",
-           "make_merge_inputs", "tiny_qkv", "rng_for"]
+           "make_merge_inputs", "tiny_qkv", "rng_for", "make_mla_inputs", "MLA_SCALE"]
 
-_KIND_PAYLOAD, _KIND_LSE, _KIND_EMPTY, _KIND_Q, _KIND_KV = 1, 2, 3, 4, 5
+_KIND_PAYLOAD, _KIND_LSE, _KIND_EMPTY, _KIND_Q, _KIND_KV, _KIND_MLA_Q, _KIND_MLA_KV = 1, 2, 3, 4, 5, 6, 7
+
+# DeepSeek-V2 MLA scores are scaled by 1/sqrt(qk_nope + qk_rope) = 1/sqrt(128 + 64)
+# before absorption; the absorbed 576-wide keys keep that scale.
+MLA_SCALE = 192 ** -0.5
 
 BF16_QNAN = 0x7FC0
 F16_QNAN = 0x7E00
@@ -155,4 +159,13 @@ def tiny_qkv(seed: int = 0, rows: int = 3, heads: int = 16, d: int = 512, tokens
     [tokens, d], both N(0, 1) float32."""
     q = rng_for(seed, _KIND_Q).standard_normal(size=(rows, heads, d), dtype=np.float32)
     kv = rng_for(seed, _KIND_KV).standard_normal(size=(tokens, d), dtype=np.float32)
+    return q, kv
+
+
+def make_mla_inputs(B: int, H: int, T: int, Dk: int = 576, seed: int = 0):
+    """Decode queries and one shard's latent KV cache, bf16 bit patterns of
+    N(0, 1) draws: q [B, H, Dk] and kv [B, T, Dk] (row b's shard-local
+    tokens)."""
+    q = bf16_bits(rng_for(seed, _KIND_MLA_Q).standard_normal(size=(B, H, Dk), dtype=np.float32))
+    kv = bf16_bits(rng_for(seed, _KIND_MLA_KV).standard_normal(size=(B, T, Dk), dtype=np.float32))
     return q, kv

@@ -1,0 +1,83 @@
+/*
+ * dcp_mla_decode_partial: the producer of the DCP partials — MLA decode
+ * attention of every query head over the tokens one context shard holds,
+ * split into up to 16 contiguous token ranges, each giving a partial output
+ * and its log-sum-exp. Their LSE-weighted merge (dcp_lse_reduce) is attention
+ * over the whole context.
+ *
+ * The operation. For row b, head h and split s over the shard's first
+ * kv_len[b] tokens (split s holds tokens [s*c, min((s+1)*c, kv_len[b])),
+ * c = ceil(kv_len[b] / n_split)):
+ *     s_t      = scale * <q[b, h, :Dk], kv[b, t, :Dk]>
+ *     out_s[b, h, :] = sum_t softmax(s)_t * kv[b, t, :Dv]     (value = first Dv dims)
+ *     lse_s[b, h]    = log_base sum_t exp(s_t)
+ *   An empty range gives out = 0 and lse = -inf.
+ *   Sources:
+ *   - "[DCP] Optimize shared Output, Query, and Indexer/Top-K via peer memory"
+ *     (sglang #32851), commit notes: under DCP each rank holds an interleaved
+ *     share of the latent KV, computes decode attention over the tokens it
+ *     owns and returns a partial output with its LSE (trtllm-gen surfaces a
+ *     base-2 LSE); attention is invariant under permuting the tokens, so any
+ *     split merges back exactly.
+ *   - "[DCP] Run fi_a2a on FlashInfer's fused all-to-all + LSE reduce"
+ *     (sglang #40539), "Speed Tests and Profiling": MLA decode with a 512-wide
+ *     latent (kv_lora_rank), 16 heads per rank; "Accuracy Tests": FlashMLA's
+ *     base-e LSE.
+ *   MLA's absorbed form attends with keys of 512 latent + 64 RoPE dims
+ *   (Dk = 576) and values of the 512 latent dims (Dv = 512) of the same
+ *   cached row; Dk = 512 (no RoPE part) is also taken.
+ *
+ * Numerics. bf16 inputs, fp32 scores and accumulation (tensor-core MMA),
+ * softmax in base 2 with the running maximum taken out, probabilities rounded
+ * to bf16 for the value product, output rounded to bf16 (round to nearest
+ * even), LSE fp32 in the requested base.
+ *
+ * Layout (all contiguous, device memory, caller-owned):
+ *   q        [B, H, Dk] bf16, 16-byte aligned
+ *   kv       [B, T, Dk] bf16, 16-byte aligned: row b's shard-local tokens
+ *   kv_len   [B] int32: tokens of row b held by this shard (clamped to [0, T])
+ *   out_ptrs host array of n_split device pointers, each [B, H, Dv] bf16,
+ *            16-byte aligned
+ *   lse_ptrs host array of n_split device pointers, each [B, H] fp32
+ *   status   NULL, or a device int32 the kernel ORs 1 into if a wait for its
+ *            own asynchronous copies ever exceeds two seconds (then the
+ *            outputs are not valid); it never hangs.
+ *
+ * Asynchrony, ownership, errors: as for dcp_lse_reduce (one kernel enqueued
+ * on `stream`, nothing allocated, graph-capturable; negative codes are host
+ * argument errors with nothing launched, positive codes are cudaError_t).
+ */
+#ifndef DCP_MLA_DECODE_H
+#define DCP_MLA_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DCP_MLA_SPLIT_MAX 16
+
+enum {
+    DCP_MLA_ERR_NULL_POINTER = -101, /* q, kv, kv_len, out_ptrs, lse_ptrs or an entry is NULL */
+    DCP_MLA_ERR_BAD_SHAPE = -102,    /* B outside [0, 65535], T < 0, H not a positive multiple of 16,
+                                        Dk not 512 or 576, or Dv not 512 */
+    DCP_MLA_ERR_BAD_SPLIT = -103,    /* n_split outside [1, DCP_MLA_SPLIT_MAX] */
+    DCP_MLA_ERR_MISALIGNED = -104,   /* q, kv or an output not 16-byte aligned, or an LSE or kv_len
+                                        pointer not 4-byte aligned */
+    DCP_MLA_ERR_BAD_FLAGS = -105     /* flag bits other than DCP_FLAG_PDL (1) */
+};
+
+int dcp_mla_decode_partial(const void* q, const void* kv, const int32_t* kv_len,
+                           int64_t B, int H, int Dk, int Dv, int64_t T, float scale, int lse_base_e,
+                           int n_split, void* const* out_ptrs, float* const* lse_ptrs,
+                           int32_t* status, unsigned flags, void* stream);
+
+/* Dynamic shared memory one CTA of the kernel uses for Dk (bytes), for sizing. */
+int dcp_mla_decode_smem_bytes(int Dk, int H);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCP_MLA_DECODE_H */

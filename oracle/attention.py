@@ -23,36 +23,41 @@ import numpy as np
 __all__ = ["attention", "split_partials"]
 
 
-def attention(q: np.ndarray, kv: np.ndarray, scale: float, base_e: bool = True):
+def attention(q: np.ndarray, kv: np.ndarray, scale: float, base_e: bool = True, dv: int | None = None):
     """Softmax attention of every query head over every token of ``kv``.
 
-    q: [R, H, Dk] queries; kv: [T, Dk] latent rows serving as both key and
-    value. Returns (o [R, H, Dk], lse [R, H]) in float64, where
-    s[r,h,t] = scale * <q[r,h], kv[t]>, o = sum_t softmax_t(s) kv[t] and
+    q: [R, H, Dk] queries; kv: [T, Dk] latent rows. The key of token t is the
+    whole row kv[t] (MLA: the 512-wide latent plus the 64-wide RoPE part); its
+    value is the first ``dv`` entries (default: the whole row). Returns
+    (o [R, H, dv], lse [R, H]) in float64, where s[r,h,t] = scale *
+    <q[r,h], kv[t]>, o = sum_t softmax_t(s) kv[t, :dv] and
     lse = log(sum_t exp(s)) (log base 2 when base_e is False). An empty token
     set gives o = 0 and lse = -inf.
     """
     q = np.asarray(q, dtype=np.float64)
     kv = np.asarray(kv, dtype=np.float64)
     R, H, _ = q.shape
+    dv = kv.shape[1] if dv is None else dv
     if kv.shape[0] == 0:
-        return np.zeros_like(q), np.full((R, H), -np.inf)
+        return np.zeros((R, H, dv)), np.full((R, H), -np.inf)
     s = scale * np.einsum("rhd,td->rht", q, kv)
-    p = np.exp(s)                       # scores are O(1) here: no shift needed in fp64
+    m = s.max(axis=-1, keepdims=True)   # log-sum-exp with the max taken out
+    p = np.exp(s - m)
     z = p.sum(axis=-1)
-    o = np.einsum("rht,td->rhd", p / z[..., None], kv)
-    lse = np.log(z)
+    o = np.einsum("rht,td->rhd", p / z[..., None], kv[:, :dv])
+    lse = m[..., 0] + np.log(z)
     if not base_e:
         lse = lse / np.log(2.0)
     return o, lse
 
 
-def split_partials(q: np.ndarray, kv: np.ndarray, shards, scale: float, base_e: bool = True):
+def split_partials(q: np.ndarray, kv: np.ndarray, shards, scale: float, base_e: bool = True,
+                   dv: int | None = None):
     """Per-shard attention: for each index array in ``shards``, attention over
-    those tokens only. Returns lists (o_j [R, H, Dk], lse_j [R, H])."""
+    those tokens only. Returns lists (o_j [R, H, dv], lse_j [R, H])."""
     outs, lses = [], []
     for idx in shards:
-        o, lse = attention(q, kv[np.asarray(idx, dtype=np.int64)], scale, base_e)
+        o, lse = attention(q, kv[np.asarray(idx, dtype=np.int64)], scale, base_e, dv)
         outs.append(o)
         lses.append(lse)
     return outs, lses

@@ -11,7 +11,8 @@ import decode_context_mla_dcp_gb300 as dcp
 from decode_context_mla_dcp_gb300 import build as dcp_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "dcp_lse_reduce.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if h.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -21,7 +22,7 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "\n".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(dcp_\w+)\s*\(", text, flags=re.M)))
 
@@ -108,3 +109,26 @@ def test_ex_rejects_bad_flags_dtype_strides(lib):
 def test_python_binding_raises_with_message(lib):
     with pytest.raises(dcp.DcpError, match="multiple of cp"):
         dcp.dcp_lse_reduce([FAKE] * 4, [FAKE] * 4, 6, 4, 1, 6, 512, True, [FAKE] * 4, stream=0)
+
+
+def test_mla_producer_rejects_bad_arguments(lib):
+    arr = ctypes.c_void_p * 2
+    outs = arr(FAKE, FAKE)
+    lses = arr(FAKE, FAKE)
+
+    def call(q=FAKE, kv=FAKE, kv_len=FAKE, B=1, H=64, Dk=576, Dv=512, T=10, n_split=2, o=outs, l=lses, status=None,
+             flags=0):
+        return lib.dcp_mla_decode_partial(q, kv, kv_len, B, H, Dk, Dv, T, 0.1, 1, n_split, o, l, status, flags,
+                                          None)
+
+    assert call(q=None) == -101
+    assert call(o=arr(FAKE, 0)) == -101
+    assert call(B=-1) == -102 and call(B=65536) == -102
+    assert call(H=8) == -102 and call(H=24) == -102
+    assert call(Dk=640) == -102 and call(Dv=256) == -102 and call(T=-1) == -102
+    assert call(n_split=0) == -103 and call(n_split=17) == -103
+    assert call(q=FAKE + 8) == -104 and call(kv_len=FAKE + 2) == -104 and call(o=arr(FAKE + 4, FAKE)) == -104
+    assert call(flags=2) == -105
+    assert call(B=0) == 0  # nothing to do, nothing launched
+    assert dcp.dcp_mla_decode_smem_bytes(576, 64) > 150000
+    assert "n_split" in dcp.dcp_lse_reduce_strerror(-103)

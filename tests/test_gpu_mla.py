@@ -1,0 +1,207 @@
+"""GPU parity of the DCP producer (split-KV MLA decode attention per shard)
+against the fp64 oracle attention, and of producer + merge against attention
+over the whole context.
+
+Tolerances: partial outputs |gpu - ref| <= 1e-2 + 8e-3*|ref| (bf16
+probabilities and bf16 output rounding dominate: about 2^-9 relative each);
+LSEs |gpu - ref| <= 1e-4 * max(|ref|, 1) (fp32 scores accumulated over
+Dk <= 576 bf16 products, hardware exp2/log2 at ~2 ulp).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import decode_context_mla_dcp_gb300 as dcp
+from decode_context_mla_dcp_gb300 import build as dcp_build
+from decode_context_mla_dcp_gb300.inputs import MLA_SCALE, bf16_bits, make_mla_inputs, tiny_qkv
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-2, 8e-3
+LSE_TOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_lib():
+    assert torch.cuda.is_available(), "the -m gpu tests need a CUDA device"
+    dcp_build.build()
+    dcp.load()
+    torch.cuda.set_device(0)
+    yield
+
+
+def dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def widen(bits):
+    return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_out(got, ref, what):
+    got = got.float().double().cpu().numpy() if torch.is_tensor(got) else got
+    assert not np.isnan(got).any(), what
+    err = np.abs(got - ref)
+    assert (err <= ATOL + RTOL * np.abs(ref)).all(), f"{what}: max err {err.max():.3g}"
+    return float(err.max())
+
+
+def check_lse(got, ref, what):
+    got = got.double().cpu().numpy() if torch.is_tensor(got) else got
+    ninf = ref == -np.inf
+    assert np.array_equal(got == -np.inf, ninf), f"{what}: -inf pattern"
+    err = np.abs(got[~ninf] - ref[~ninf])
+    assert (err <= LSE_TOL * np.maximum(np.abs(ref[~ninf]), 1)).all(), f"{what}: LSE max err {err.max():.3g}"
+    return float(err.max()) if err.size else 0.0
+
+
+def oracle_partials(q_bits, kv_bits, lens, n_split, scale, base_e, dv=512):
+    """Oracle per (row, split): attention over the split's token range."""
+    from oracle.attention import attention
+    q = widen(q_bits)
+    kv = widen(kv_bits)
+    B, H, _ = q.shape
+    outs = [np.zeros((B, H, dv)) for _ in range(n_split)]
+    lses = [np.full((B, H), -np.inf) for _ in range(n_split)]
+    for b in range(B):
+        L = int(lens[b])
+        chunk = -(-L // n_split)
+        for s in range(n_split):
+            t0, t1 = s * chunk, min(L, (s + 1) * chunk)
+            if t1 > t0:
+                o, l = attention(q[b:b + 1], kv[b, t0:t1], scale, base_e, dv)
+                outs[s][b], lses[s][b] = o[0], l[0]
+    return outs, lses
+
+
+@pytest.mark.parametrize("H,Dk,T,n_split", [(16, 576, 100, 1), (64, 576, 257, 3), (128, 576, 96, 2),
+                                            (32, 512, 64, 1), (16, 512, 33, 16)])
+@pytest.mark.parametrize("base_e", [True, False])
+def test_partials_match_oracle(oracle_mod, H, Dk, T, n_split, base_e):
+    B = 4
+    q, kv = make_mla_inputs(B, H, T, Dk, seed=H + T)
+    lens = np.array([T, 1, 0, T - 5 if T > 5 else T], dtype=np.int32)
+    outs, lses = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), torch.from_numpy(lens).cuda(), MLA_SCALE,
+                                        lse_base_e=base_e, n_split=n_split)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle_partials(q, kv, lens, n_split, MLA_SCALE, base_e)
+    for s in range(n_split):
+        check_out(outs[s], ref_o[s], f"split {s}")
+        check_lse(lses[s], ref_l[s], f"split {s}")
+
+
+def test_tiny_exactness_producer_then_merge(oracle_mod):
+    """The tiny exactness check end to end on the GPU: two shards of 32
+    tokens each, producer per shard, merge; equals attention over all 64."""
+    from oracle.attention import attention
+    q32, kv32 = tiny_qkv(0)
+    q = bf16_bits(q32)                                   # [3, 16, 512]
+    kv = np.broadcast_to(bf16_bits(kv32), (3, 64, 512)).copy()
+    scale = 1 / math.sqrt(512)
+    parts, part_l = [], []
+    for j in range(2):
+        o, l = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv[:, 32 * j:32 * j + 32].copy()),
+                                      torch.full((3,), 32, dtype=torch.int32, device="cuda"), scale)
+        parts.append(o[0])
+        part_l.append(l[0])
+    outs, louts = dcp.merge(parts, part_l, True)
+    torch.cuda.synchronize()
+    o_full, l_full = attention(widen(q), widen(kv[0]), scale)
+    check_out(torch.cat(outs, 1), o_full, "tiny merged output")
+    check_lse(torch.cat(louts, 1), l_full, "tiny merged LSE")
+
+
+@pytest.mark.parametrize("cp,n_split,H", [(4, 2, 64), (8, 2, 128), (2, 8, 16)])
+def test_dcp_composition_equals_full_attention(oracle_mod, cp, n_split, H):
+    """Interleaved context shards (token t on shard t % cp), producer per
+    shard with in-shard splits, one merge over all cp*n_split partials into a
+    single [B, H, 512] output: attention over every row's whole context."""
+    from oracle.attention import attention
+    B, L_max, Dk = 3, 300, 576
+    q, kv_full = make_mla_inputs(B, H, L_max, Dk, seed=cp * 10 + n_split)
+    L = np.array([L_max, 37, cp - 1], dtype=np.int32)  # the last row leaves one shard empty
+    parts, part_l = [], []
+    for j in range(cp):
+        T_j = -(-L_max // cp)
+        kv_j = np.zeros((B, T_j, Dk), dtype=np.uint16)
+        lens_j = np.zeros(B, dtype=np.int32)
+        for b in range(B):
+            own = np.arange(j, L[b], cp)
+            kv_j[b, :own.size] = kv_full[b, own]
+            lens_j[b] = own.size
+        o, l = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv_j), torch.from_numpy(lens_j).cuda(), MLA_SCALE,
+                                      n_split=n_split)
+        parts += o
+        part_l += l
+    n_src = cp * n_split
+    assert n_src <= 16 and H % n_src == 0
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    Hs = H // n_src
+    # destination r of the merge = heads [r*Hs, (r+1)*Hs) of one contiguous output
+    dcp.dcp_lse_reduce_ex(parts, part_l, n_src, B, H, 512, True, dcp.DCP_DTYPE_BF16,
+                          [out.data_ptr() + r * Hs * 512 * 2 for r in range(n_src)],
+                          [lse.data_ptr() + r * Hs * 4 for r in range(n_src)],
+                          layout=dcp.Layout(src_row=H * 512, src_head=512, lse_row=H, lse_head=1,
+                                            dst_row=H * 512, dst_head=512, lse_out_row=H))
+    torch.cuda.synchronize()
+    for b in range(B):
+        o_ref, l_ref = attention(widen(q[b:b + 1]), widen(kv_full[b, :L[b]]), MLA_SCALE, dv=512)
+        check_out(out[b:b + 1], o_ref, f"row {b}")
+        check_lse(lse[b:b + 1], l_ref, f"row {b}")
+
+
+def test_empty_shard_and_status_and_determinism():
+    B, H, T = 2, 64, 80
+    q, kv = make_mla_inputs(B, H, T, 576, seed=7)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lens = torch.tensor([0, 80], dtype=torch.int32, device="cuda")
+    o1, l1 = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), lens, MLA_SCALE, n_split=2, status=status)
+    o2, l2 = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), lens, MLA_SCALE, n_split=2, status=status,
+                                    flags=dcp.DCP_FLAG_PDL)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for s in range(2):
+        assert (o1[s][0] == 0).all() and (l1[s][0] == -float("inf")).all()
+        assert torch.equal(o1[s].view(torch.int16), o2[s].view(torch.int16))
+        assert torch.equal(l1[s].view(torch.int32), l2[s].view(torch.int32))
+
+
+def test_lengths_beyond_the_cache_are_clamped(oracle_mod):
+    B, H, T = 2, 16, 40
+    q, kv = make_mla_inputs(B, H, T, 576, seed=9)
+    lens = np.array([1000, -3], dtype=np.int32)
+    outs, lses = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), torch.from_numpy(lens).cuda(), MLA_SCALE)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle_partials(q, kv, np.array([T, 0]), 1, MLA_SCALE, True)
+    check_out(outs[0], ref_o[0], "clamped")
+    check_lse(lses[0], ref_l[0], "clamped")
+
+
+def test_graph_capture_of_producer_and_merge():
+    B, H, T, cp = 2, 64, 128, 2
+    q, kv = make_mla_inputs(B, H, T, 576, seed=11)
+    qd, kvd = dev_bf16(q), dev_bf16(kv)
+    lens = torch.tensor([128, 77], dtype=torch.int32, device="cuda")
+    parts = [torch.empty((B, H, 512), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
+    pl = [torch.empty((B, H), dtype=torch.float32, device="cuda") for _ in range(cp)]
+    outs = [torch.empty((B, H // cp, 512), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
+    louts = [torch.empty((B, H // cp), dtype=torch.float32, device="cuda") for _ in range(cp)]
+
+    def step():
+        dcp.mla_decode_partial(qd, kvd, lens, MLA_SCALE, n_split=cp, outs=parts, lses=pl, flags=dcp.DCP_FLAG_PDL)
+        dcp.merge(parts, pl, True, outs=outs, lse_outs=louts, flags=dcp.DCP_FLAG_PDL)
+
+    step()
+    torch.cuda.synchronize()
+    ref = [o.clone() for o in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for o in outs:
+        o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(ref, outs))

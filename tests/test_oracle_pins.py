@@ -369,3 +369,49 @@ def test_long_contexts_mask_nothing(oracle_mod):
     b, lb = oracle_mod.merge(inp.srcs, inp.lses, True, seq_lens=np.array([64, 100, 1 << 20, 65]), interleave=8)
     for r in range(8):
         assert np.array_equal(a[r], b[r]) and np.array_equal(la[r], lb[r])
+
+
+# --- the attention oracle (producer of the partials) ------------------------------
+
+def test_attention_over_one_token_is_that_value():
+    # softmax over a single token is 1: o = v, lse = s
+    from oracle.attention import attention
+    rng = np.random.default_rng(51)
+    q = rng.standard_normal((2, 3, 576))
+    kv = rng.standard_normal((1, 576))
+    o, lse = attention(q, kv, 0.1, dv=512)
+    assert np.array_equal(o, np.broadcast_to(kv[0, :512], (2, 3, 512)))
+    np.testing.assert_allclose(lse, 0.1 * np.einsum("rhd,d->rh", q, kv[0]), rtol=1e-14)
+
+
+def test_attention_with_zero_query_is_the_value_mean():
+    # q = 0 gives equal scores: o = mean of the value rows, lse = log(T)
+    from oracle.attention import attention
+    rng = np.random.default_rng(53)
+    kv = rng.standard_normal((37, 576))
+    o, lse = attention(np.zeros((1, 2, 576)), kv, 0.3, dv=512)
+    np.testing.assert_allclose(o[0, 1], kv[:, :512].mean(0), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(lse, np.log(37.0), rtol=1e-15)
+    _, lse2 = attention(np.zeros((1, 2, 576)), kv, 0.3, base_e=False, dv=512)
+    np.testing.assert_allclose(lse2, np.log2(37.0), rtol=1e-15)
+
+
+def test_attention_two_tokens_closed_form():
+    # two tokens with scores 0 and ln 3: weights 1/4 and 3/4
+    from oracle.attention import attention
+    q = np.zeros((1, 1, 4)); q[0, 0, 0] = 1.0
+    kv = np.array([[0.0, 1.0, 2.0, 9.0], [math.log(3.0), 5.0, -2.0, 9.0]])
+    o, lse = attention(q, kv, 1.0, dv=3)
+    np.testing.assert_allclose(o[0, 0], [0.75 * math.log(3.0), 0.25 * 1 + 0.75 * 5, 0.25 * 2 - 0.75 * 2], rtol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], math.log(4.0), rtol=1e-15)
+
+
+def test_attention_is_invariant_under_token_permutation():
+    from oracle.attention import attention
+    rng = np.random.default_rng(55)
+    q = rng.standard_normal((2, 4, 64)); kv = rng.standard_normal((20, 64))
+    perm = rng.permutation(20)
+    o1, l1 = attention(q, kv, 0.2, dv=48)
+    o2, l2 = attention(q, kv[perm], 0.2, dv=48)
+    np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(l1, l2, rtol=1e-14)
