@@ -17,10 +17,12 @@ from __future__ import annotations
 from ._binding import (DCP_DTYPE_BF16, DCP_DTYPE_F16, DCP_FLAG_LSE_FIRST, DCP_FLAG_PDL, DCP_FLAG_PRELOAD,
                        DCP_LSE_REDUCE_CP_MAX, DCP_MLA_SPLIT_MAX, EXPORTED_SYMBOLS, DcpError, Layout,
                        dcp_lse_reduce, dcp_lse_reduce_ex, dcp_lse_reduce_strerror, dcp_lse_reduce_version,
-                       dcp_mla_decode_partial, dcp_mla_decode_smem_bytes, library_path, load)
+                       dcp_mla_decode, dcp_mla_decode_partial, dcp_mla_decode_smem_bytes,
+                       dcp_mla_decode_workspace_bytes, library_path, load)
 
 __all__ = ["dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dcp_lse_reduce_version", "merge",
            "dcp_mla_decode_partial", "dcp_mla_decode_smem_bytes", "mla_decode_partial", "DCP_MLA_SPLIT_MAX",
+           "dcp_mla_decode", "dcp_mla_decode_workspace_bytes", "mla_decode_dcp",
            "algorithmic_bytes", "Layout", "DcpError", "load", "library_path", "EXPORTED_SYMBOLS",
            "DCP_DTYPE_BF16", "DCP_DTYPE_F16", "DCP_FLAG_PDL", "DCP_FLAG_PRELOAD", "DCP_FLAG_LSE_FIRST",
            "DCP_LSE_REDUCE_CP_MAX"]
@@ -114,3 +116,29 @@ def mla_decode_partial(q, kv, kv_len, scale: float, *, lse_base_e: bool = True, 
     dcp_mla_decode_partial(q, kv, kv_len, B, H, Dk, dv, T, scale, lse_base_e, n_split, outs, lses, status=status,
                            flags=flags, stream=stream)
     return outs, lses
+
+
+def mla_decode_dcp(q, kvs, kv_lens, scale: float, *, n_split: int = 1, lse_base_e: bool = True, dv: int = 512,
+                   workspace=None, outs=None, lse_outs=None, status=None, flags: int = 0, stream=None):
+    """DCP decode attention on one GPU: the producer over each shard in
+    ``kvs`` (bf16 [B, T, Dk] each, token counts ``kv_lens`` int32 [B] each),
+    then the merge into cp destinations. Returns (outs, lse_outs): cp bf16
+    [B, H/cp, dv] and cp fp32 [B, H/cp]. The workspace (a uint8 CUDA tensor of
+    at least dcp_mla_decode_workspace_bytes bytes) is allocated with torch
+    when not given."""
+    import torch
+
+    cp = len(kvs)
+    B, H, Dk = q.shape
+    T = kvs[0].shape[1]
+    need = dcp_mla_decode_workspace_bytes(cp, n_split, B, H, dv)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
+    if outs is None:
+        outs = [torch.empty((B, H // cp, dv), dtype=torch.bfloat16, device=q.device) for _ in range(cp)]
+    if lse_outs is None:
+        lse_outs = [torch.empty((B, H // cp), dtype=torch.float32, device=q.device) for _ in range(cp)]
+    dcp_mla_decode(q, kvs, kv_lens, cp, B, H, Dk, dv, T, scale, lse_base_e, n_split, workspace,
+                   workspace.numel() * workspace.element_size(), outs, lse_outs, status=status, flags=flags,
+                   stream=stream)
+    return outs, lse_outs

@@ -23,13 +23,16 @@ DCP_FLAG_PRELOAD = 2
 DCP_FLAG_LSE_FIRST = 4
 
 EXPORTED_SYMBOLS = ("dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dcp_lse_reduce_version",
-                    "dcp_mla_decode_partial", "dcp_mla_decode_smem_bytes")
+                    "dcp_mla_decode_partial", "dcp_mla_decode_smem_bytes", "dcp_mla_decode_workspace_bytes",
+                    "dcp_mla_decode")
 DCP_MLA_SPLIT_MAX = 16
 _MLA_ERRORS = {-101: "q, kv, kv_len, out_ptrs, lse_ptrs or an entry is NULL",
                -102: "B must be in [0, 65535], T >= 0, H a positive multiple of 16, Dk 512 or 576, Dv 512",
                -103: "n_split must be in [1, 16]",
                -104: "q, kv and outputs must be 16-byte aligned; LSE, kv_len and status 4-byte aligned",
-               -105: "only DCP_FLAG_PDL is accepted"}
+               -105: "only DCP_FLAG_PDL is accepted",
+               -106: "workspace is NULL, not 256-byte aligned, or smaller than dcp_mla_decode_workspace_bytes",
+               -107: "cp*n_split must be <= 16 and divide H"}
 DCP_LSE_REDUCE_INTERLEAVE_MAX = 1 << 24
 
 
@@ -84,6 +87,12 @@ def load(path: str | None = None):
         lib.dcp_mla_decode_partial.restype = ci
         lib.dcp_mla_decode_smem_bytes.argtypes = [ci, ci]
         lib.dcp_mla_decode_smem_bytes.restype = ci
+        lib.dcp_mla_decode_workspace_bytes.argtypes = [ci, ci, i64, ci, ci]
+        lib.dcp_mla_decode_workspace_bytes.restype = i64
+        lib.dcp_mla_decode.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ci, i64, ci, ci, ci, i64,
+                                       ctypes.c_float, ci, ci, vp, i64, ctypes.POINTER(vp), ctypes.POINTER(vp), vp,
+                                       ctypes.c_uint, vp]
+        lib.dcp_mla_decode.restype = ci
         if path is None:
             _lib = lib
         return lib
@@ -166,6 +175,22 @@ def dcp_mla_decode_partial(q, kv, kv_len, B: int, H: int, Dk: int, Dv: int, T: i
 
 def dcp_mla_decode_smem_bytes(Dk: int, H: int) -> int:
     return int(load().dcp_mla_decode_smem_bytes(int(Dk), int(H)))
+
+
+def dcp_mla_decode_workspace_bytes(cp: int, n_split: int, B: int, H: int, Dv: int = 512) -> int:
+    return int(load().dcp_mla_decode_workspace_bytes(int(cp), int(n_split), int(B), int(H), int(Dv)))
+
+
+def dcp_mla_decode(q, kv_ptrs, kv_len_ptrs, cp: int, B: int, H: int, Dk: int, Dv: int, T: int, scale: float,
+                   lse_base_e: bool, n_split: int, workspace, workspace_bytes: int, dst_ptrs, lse_out_ptrs=None,
+                   status=None, flags: int = 0, stream=None) -> None:
+    """Producer over cp shards + merge into cp destinations (see include/dcp_mla_decode.h)."""
+    lib = load()
+    _check(lib.dcp_mla_decode(_ptr(q), _ptr_array(kv_ptrs, cp), _ptr_array(kv_len_ptrs, cp), int(cp), int(B),
+                              int(H), int(Dk), int(Dv), int(T), float(scale), 1 if lse_base_e else 0, int(n_split),
+                              _ptr(workspace), int(workspace_bytes), _ptr_array(dst_ptrs, cp),
+                              _ptr_array(lse_out_ptrs, cp, allow_none=True), _ptr(status), int(flags),
+                              _stream(stream)))
 
 
 def dcp_lse_reduce_version() -> int:

@@ -15,7 +15,7 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "dcp_lse_reduce.cu"), os.path.join(PKG, "csrc", "mla_decode_partial.cu")]
+SOURCES = [os.path.join(PKG, "csrc", name) for name in ("dcp_lse_reduce.cu", "mla_decode_partial.cu")]
 HEADERS = [os.path.join(ROOT, "include", "dcp_lse_reduce.h"), os.path.join(ROOT, "include", "dcp_mla_decode.h")]
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libdcp_lse_reduce.so"

@@ -65,7 +65,10 @@ enum {
     DCP_MLA_ERR_BAD_SPLIT = -103,    /* n_split outside [1, DCP_MLA_SPLIT_MAX] */
     DCP_MLA_ERR_MISALIGNED = -104,   /* q, kv or an output not 16-byte aligned, or an LSE or kv_len
                                         pointer not 4-byte aligned */
-    DCP_MLA_ERR_BAD_FLAGS = -105     /* flag bits other than DCP_FLAG_PDL (1) */
+    DCP_MLA_ERR_BAD_FLAGS = -105,    /* flag bits other than DCP_FLAG_PDL (1) */
+    DCP_MLA_ERR_WORKSPACE = -106,    /* workspace NULL, not 256-byte aligned, or smaller than
+                                        dcp_mla_decode_workspace_bytes(...) */
+    DCP_MLA_ERR_BAD_CP = -107        /* cp < 1, cp*n_split > 16, or H not a multiple of cp*n_split */
 };
 
 int dcp_mla_decode_partial(const void* q, const void* kv, const int32_t* kv_len,
@@ -75,6 +78,40 @@ int dcp_mla_decode_partial(const void* q, const void* kv, const int32_t* kv_len,
 
 /* Dynamic shared memory one CTA of the kernel uses for Dk (bytes), for sizing. */
 int dcp_mla_decode_smem_bytes(int Dk, int H);
+
+/*
+ * Bytes of caller-provided workspace dcp_mla_decode needs: the cp*n_split
+ * partial outputs ([B, H, Dv] bf16 each) and LSEs ([B, H] fp32 each).
+ * Returns -1 for a negative or overflowing size.
+ */
+int64_t dcp_mla_decode_workspace_bytes(int cp, int n_split, int64_t B, int H, int Dv);
+
+/*
+ * DCP decode attention on one GPU: dcp_mla_decode_partial over each of cp
+ * context shards (kv_ptrs[j], kv_len_ptrs[j]: shard j's [B, T, Dk] cache and
+ * [B] token counts, each row's tokens split into n_split ranges), then the
+ * LSE-weighted merge (dcp_lse_reduce) of all cp*n_split partials, in which
+ * destination r receives heads [r*H/cp, (r+1)*H/cp):
+ *   dst_ptrs[r]      [B, H/cp, Dv] bf16, 16-byte aligned
+ *   lse_out_ptrs     NULL, or cp pointers to [B, H/cp] fp32 merged LSEs (an
+ *                    entry may be NULL)
+ *   workspace        device memory of at least
+ *                    dcp_mla_decode_workspace_bytes(cp, n_split, B, H, Dv)
+ *                    bytes, 256-byte aligned, owned by the caller; its
+ *                    contents on entry do not matter. Calls that share a
+ *                    workspace must be ordered (one stream, or events).
+ * The result is attention over every row's whole context (the union of the
+ * shards' tokens): "[DCP] Optimize shared Output, Query, and Indexer/Top-K via
+ * peer memory" (sglang #32851), commit notes on the interleaved KV shards and
+ * the cross-rank combine; on one GPU the shards are local buffers and the
+ * exchange is the merge's strided read. cp launches of the producer and one
+ * merge are enqueued on `stream` (PDL between them with DCP_FLAG_PDL).
+ * Constraints: cp*n_split <= 16 and H a multiple of cp*n_split and of 16.
+ */
+int dcp_mla_decode(const void* q, const void* const* kv_ptrs, const int32_t* const* kv_len_ptrs, int cp,
+                   int64_t B, int H, int Dk, int Dv, int64_t T, float scale, int lse_base_e, int n_split,
+                   void* workspace, int64_t workspace_bytes, void* const* dst_ptrs, float* const* lse_out_ptrs,
+                   int32_t* status, unsigned flags, void* stream);
 
 #ifdef __cplusplus
 }

@@ -132,3 +132,23 @@ def test_mla_producer_rejects_bad_arguments(lib):
     assert call(B=0) == 0  # nothing to do, nothing launched
     assert dcp.dcp_mla_decode_smem_bytes(576, 64) > 150000
     assert "n_split" in dcp.dcp_lse_reduce_strerror(-103)
+
+
+def test_fused_decode_rejects_bad_workspace_and_cp(lib):
+    need = dcp.dcp_mla_decode_workspace_bytes(4, 2, 3, 64)
+    assert need == 8 * (3 * 64 * 512 * 2 + 768)  # both parts are already multiples of 256 bytes
+    arr = ctypes.c_void_p * 4
+    kv = arr(FAKE, FAKE, FAKE, FAKE)
+    lens = arr(FAKE, FAKE, FAKE, FAKE)
+    dst = arr(FAKE, FAKE, FAKE, FAKE)
+
+    def call(cp=4, n_split=2, H=64, ws=FAKE, ws_bytes=None):
+        return lib.dcp_mla_decode(FAKE, kv, lens, cp, 3, H, 576, 512, 100, 0.1, 1, n_split, ws,
+                                  need if ws_bytes is None else ws_bytes, dst, None, None, 0, None)
+
+    assert call(ws_bytes=need - 1) == -106
+    assert call(ws=FAKE + 128) == -106
+    assert call(ws=None) == -106
+    assert call(n_split=8) == -107          # 4 * 8 sources > 16
+    assert call(H=36) == -107               # 36 % 8 != 0
+    assert call(cp=0) == -107

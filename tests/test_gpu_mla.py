@@ -205,3 +205,67 @@ def test_graph_capture_of_producer_and_merge():
     g.replay()
     torch.cuda.synchronize()
     assert all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(ref, outs))
+
+
+def _interleaved_shards(kv_full, L, cp):
+    """Shard j holds tokens j, j+cp, ... of every row (interleave 1)."""
+    B, L_max, Dk = kv_full.shape
+    T = -(-L_max // cp)
+    kvs, lens = [], []
+    for j in range(cp):
+        kv_j = np.zeros((B, T, Dk), dtype=np.uint16)
+        n_j = np.zeros(B, dtype=np.int32)
+        for b in range(B):
+            own = np.arange(j, L[b], cp)
+            kv_j[b, :own.size] = kv_full[b, own]
+            n_j[b] = own.size
+        kvs.append(dev_bf16(kv_j))
+        lens.append(torch.from_numpy(n_j).cuda())
+    return kvs, lens
+
+
+@pytest.mark.parametrize("cp,n_split,H,Dk", [(4, 2, 64, 576), (8, 2, 128, 576), (2, 4, 16, 512), (1, 16, 16, 576)])
+def test_fused_dcp_decode_equals_full_attention(oracle_mod, cp, n_split, H, Dk):
+    from oracle.attention import attention
+    B, L_max = 3, 260
+    q, kv_full = make_mla_inputs(B, H, L_max, Dk, seed=cp * 100 + n_split)
+    L = np.array([L_max, 41, max(cp - 1, 1)], dtype=np.int32)
+    kvs, lens = _interleaved_shards(kv_full, L, cp)
+    outs, louts = dcp.mla_decode_dcp(dev_bf16(q), kvs, lens, MLA_SCALE, n_split=n_split)
+    torch.cuda.synchronize()
+    Hl = H // cp
+    for b in range(B):
+        o_ref, l_ref = attention(widen(q[b:b + 1]), widen(kv_full[b, :L[b]]), MLA_SCALE, dv=512)
+        for r in range(cp):
+            check_out(outs[r][b:b + 1], o_ref[:, r * Hl:(r + 1) * Hl], f"row {b} dest {r}")
+            check_lse(louts[r][b:b + 1], l_ref[:, r * Hl:(r + 1) * Hl], f"row {b} dest {r}")
+
+
+def test_fused_dcp_decode_graph_replay_and_workspace_reuse():
+    B, H, L_max, cp, n_split = 2, 64, 200, 4, 2
+    q, kv_full = make_mla_inputs(B, H, L_max, 576, seed=3)
+    kvs, lens = _interleaved_shards(kv_full, np.array([200, 150], dtype=np.int32), cp)
+    qd = dev_bf16(q)
+    ws = torch.empty((dcp.dcp_mla_decode_workspace_bytes(cp, n_split, B, H),), dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((B, H // cp, 512), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
+    louts = [torch.empty((B, H // cp), dtype=torch.float32, device="cuda") for _ in range(cp)]
+
+    def call():
+        dcp.mla_decode_dcp(qd, kvs, lens, MLA_SCALE, n_split=n_split, workspace=ws, outs=outs, lse_outs=louts,
+                           flags=dcp.DCP_FLAG_PDL)
+
+    call()
+    torch.cuda.synchronize()
+    ref = [o.clone() for o in outs] + [l.clone() for l in louts]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+        call()  # the same workspace, in stream order
+    for t in outs + louts:
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    got = outs + louts
+    assert all(torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
+               for a, b in zip(ref, got))
