@@ -24,7 +24,8 @@ DCP_FLAG_LSE_FIRST = 4
 
 EXPORTED_SYMBOLS = ("dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dcp_lse_reduce_version",
                     "dcp_mla_decode_partial", "dcp_mla_decode_smem_bytes", "dcp_mla_decode_workspace_bytes",
-                    "dcp_mla_decode")
+                    "dcp_mla_decode", "dcp_mla_decode_noalloc")
+DCP_MLA_NOALLOC_SCRATCH_BYTES = 32 << 20
 DCP_MLA_SPLIT_MAX = 16
 _MLA_ERRORS = {-101: "q, kv, kv_len, out_ptrs, lse_ptrs or an entry is NULL",
                -102: "B must be in [0, 65535], T >= 0, H a positive multiple of 16, Dk 512 or 576, Dv 512",
@@ -32,7 +33,9 @@ _MLA_ERRORS = {-101: "q, kv, kv_len, out_ptrs, lse_ptrs or an entry is NULL",
                -104: "q, kv and outputs must be 16-byte aligned; LSE, kv_len and status 4-byte aligned",
                -105: "only DCP_FLAG_PDL is accepted",
                -106: "workspace is NULL, not 256-byte aligned, or smaller than dcp_mla_decode_workspace_bytes",
-               -107: "cp*n_split must be <= 16 and divide H"}
+               -107: "cp*n_split must be <= 16 and divide H",
+               -108: "the partials need more than the built-in 32 MiB scratch (DCP_MLA_NOALLOC_SCRATCH_BYTES)",
+               -109: "the built-in scratch array's device address could not be obtained on this device"}
 DCP_LSE_REDUCE_INTERLEAVE_MAX = 1 << 24
 
 
@@ -93,6 +96,10 @@ def load(path: str | None = None):
                                        ctypes.c_float, ci, ci, vp, i64, ctypes.POINTER(vp), ctypes.POINTER(vp), vp,
                                        ctypes.c_uint, vp]
         lib.dcp_mla_decode.restype = ci
+        lib.dcp_mla_decode_noalloc.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ci, i64, ci, ci, ci, i64,
+                                               ctypes.c_float, ci, ci, ctypes.POINTER(vp), ctypes.POINTER(vp), vp,
+                                               ctypes.c_uint, vp]
+        lib.dcp_mla_decode_noalloc.restype = ci
         if path is None:
             _lib = lib
         return lib
@@ -195,3 +202,18 @@ def dcp_mla_decode(q, kv_ptrs, kv_len_ptrs, cp: int, B: int, H: int, Dk: int, Dv
 
 def dcp_lse_reduce_version() -> int:
     return int(load().dcp_lse_reduce_version())
+
+
+def dcp_mla_decode_noalloc(q, kv_ptrs, kv_len_ptrs, cp: int, B: int, H: int, Dk: int, Dv: int, T: int,
+                           scale: float, lse_base_e: bool, n_split: int, dst_ptrs, lse_out_ptrs=None, status=None,
+                           flags: int = 0, stream=None) -> None:
+    """dcp_mla_decode with the partials in the library's built-in scratch
+    array instead of a caller workspace, for callers that cannot allocate
+    device memory when they decode (see include/dcp_mla_decode.h: the limit,
+    the first-call set-up, and why overlapping calls race)."""
+    lib = load()
+    _check(lib.dcp_mla_decode_noalloc(_ptr(q), _ptr_array(kv_ptrs, cp), _ptr_array(kv_len_ptrs, cp), int(cp), int(B),
+                                      int(H), int(Dk), int(Dv), int(T), float(scale), 1 if lse_base_e else 0,
+                                      int(n_split), _ptr_array(dst_ptrs, cp),
+                                      _ptr_array(lse_out_ptrs, cp, allow_none=True), _ptr(status), int(flags),
+                                      _stream(stream)))

@@ -25,6 +25,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "dcp_lse_reduce.h"
 #include "dcp_mla_decode.h"
 
@@ -532,4 +534,53 @@ extern "C" int dcp_mla_decode(const void* q, const void* const* kv_ptrs, const i
     lay.lse_out_row = Hl;
     return dcp_lse_reduce_ex(part_out, part_lse, n_src, B, H, Dv, lse_base_e, DCP_DTYPE_BF16, dst, lout, &lay, nullptr,
                              1, flags & DCP_FLAG_PDL, stream);
+}
+
+// ---- the no-allocation variant -----------------------------------------------------
+
+namespace {
+
+// Scratch for dcp_mla_decode_noalloc: the partials of one call. Host code must
+// not use this name as an address; it takes the device address from
+// cudaGetSymbolAddress on each device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[DCP_MLA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once.
+void* scratch_on_current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        g_scratch_ptr[dev] = ptr;
+    }
+    return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" int dcp_mla_decode_noalloc(const void* q, const void* const* kv_ptrs, const int32_t* const* kv_len_ptrs,
+                                      int cp, int64_t B, int H, int Dk, int Dv, int64_t T, float scale,
+                                      int lse_base_e, int n_split, void* const* dst_ptrs, float* const* lse_out_ptrs,
+                                      int32_t* status, unsigned flags, void* stream) {
+    if (n_split < 1 || n_split > DCP_MLA_SPLIT_MAX) return DCP_MLA_ERR_BAD_SPLIT;
+    if (cp < 1 || cp * n_split > DCP_LSE_REDUCE_CP_MAX || H < 1 || H % (cp * n_split) != 0) return DCP_MLA_ERR_BAD_CP;
+    const int64_t need = dcp_mla_decode_workspace_bytes(cp, n_split, B, H, Dv);
+    if (need < 0) return DCP_MLA_ERR_BAD_SHAPE;
+    if (need > (int64_t)DCP_MLA_NOALLOC_SCRATCH_BYTES) return DCP_MLA_ERR_SCRATCH_LIMIT;
+    void* scratch = scratch_on_current_device();
+    if (scratch == nullptr) return DCP_MLA_ERR_SCRATCH_SETUP;
+    return dcp_mla_decode(q, kv_ptrs, kv_len_ptrs, cp, B, H, Dk, Dv, T, scale, lse_base_e, n_split, scratch,
+                          DCP_MLA_NOALLOC_SCRATCH_BYTES, dst_ptrs, lse_out_ptrs, status, flags, stream);
 }

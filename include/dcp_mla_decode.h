@@ -68,7 +68,11 @@ enum {
     DCP_MLA_ERR_BAD_FLAGS = -105,    /* flag bits other than DCP_FLAG_PDL (1) */
     DCP_MLA_ERR_WORKSPACE = -106,    /* workspace NULL, not 256-byte aligned, or smaller than
                                         dcp_mla_decode_workspace_bytes(...) */
-    DCP_MLA_ERR_BAD_CP = -107        /* cp < 1, cp*n_split > 16, or H not a multiple of cp*n_split */
+    DCP_MLA_ERR_BAD_CP = -107,       /* cp < 1, cp*n_split > 16, or H not a multiple of cp*n_split */
+    DCP_MLA_ERR_SCRATCH_LIMIT = -108, /* dcp_mla_decode_noalloc: the partials need more than
+                                         DCP_MLA_NOALLOC_SCRATCH_BYTES */
+    DCP_MLA_ERR_SCRATCH_SETUP = -109  /* dcp_mla_decode_noalloc: the scratch array's device address
+                                         could not be obtained on the current device */
 };
 
 int dcp_mla_decode_partial(const void* q, const void* kv, const int32_t* kv_len,
@@ -112,6 +116,42 @@ int dcp_mla_decode(const void* q, const void* const* kv_ptrs, const int32_t* con
                    int64_t B, int H, int Dk, int Dv, int64_t T, float scale, int lse_base_e, int n_split,
                    void* workspace, int64_t workspace_bytes, void* const* dst_ptrs, float* const* lse_out_ptrs,
                    int32_t* status, unsigned flags, void* stream);
+
+/*
+ * Capacity of the library's built-in scratch array used by
+ * dcp_mla_decode_noalloc (bytes): 32 MiB.
+ */
+#define DCP_MLA_NOALLOC_SCRATCH_BYTES (32 << 20)
+
+/*
+ * dcp_mla_decode without a workspace argument, for callers that cannot
+ * allocate device memory when they run the decode: for instance code inside a
+ * host process whose device memory is fully reserved by another allocator at
+ * start-up, plug-in or embedded runtimes that forbid allocation after
+ * initialisation, or latency-critical paths that cannot afford cudaMalloc's
+ * implicit device synchronisation. (The pages this library follows have no
+ * counterpart to this call; it is a deployment convenience.)
+ *
+ * The partial outputs and LSEs live in one scratch array of
+ * DCP_MLA_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU
+ * that loads the library holds until the process exits. Arguments and
+ * results are as for dcp_mla_decode; the call needs
+ * dcp_mla_decode_workspace_bytes(cp, n_split, B, H, Dv) <=
+ * DCP_MLA_NOALLOC_SCRATCH_BYTES, else it returns DCP_MLA_ERR_SCRATCH_LIMIT
+ * and enqueues nothing. It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (the calling thread's current device) and keeps it; make that first
+ * call outside any stream capture. The array is shared by every call on a
+ * device and keeps the last call's contents (nothing in it has to start at
+ * zero); calls whose work overlaps on the GPU — on different streams without
+ * ordering between them — race on it and give undefined results.
+ */
+int dcp_mla_decode_noalloc(const void* q, const void* const* kv_ptrs, const int32_t* const* kv_len_ptrs, int cp,
+                           int64_t B, int H, int Dk, int Dv, int64_t T, float scale, int lse_base_e, int n_split,
+                           void* const* dst_ptrs, float* const* lse_out_ptrs, int32_t* status, unsigned flags,
+                           void* stream);
 
 #ifdef __cplusplus
 }
