@@ -42,6 +42,7 @@ if ROOT not in sys.path:
 METRIC = "LSE-combine HBM GB/s (% of peak) and µs/call at rows 1–128, 1×GB300"
 CALLS_PER_GRAPH = 60
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCE = os.path.join(ROOT, "decode_context_mla_dcp_gb300", "csrc", "dcp_lse_reduce.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
@@ -77,6 +78,15 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s: the measured burst figure, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS
 
 
 def kernel_source_sha():
@@ -339,6 +349,73 @@ def stress_extra(peak):
             "frac_of_measured_peak": round(gbs / peak, 4)}
 
 
+def mla_extras(hbm_peak, tensor_peak):
+    """The DCP producer (split-KV MLA decode attention over one shard) and the
+    fused single-GPU decode (producer over cp shards + merge), timed on
+    DeepSeek-V2-shaped (128 heads) and Kimi-K2.5-shaped (64 heads) shards:
+    Dk = 576 (512 latent + 64 RoPE), Dv = 512, bf16, 4096 shard tokens per row,
+    8 rows. Ten calls per CUDA graph, each on its own KV cache (cold: 377 MB
+    of caches > L2). Inputs drawn on the device with a seeded generator
+    (timing only)."""
+    import torch
+    import decode_context_mla_dcp_gb300 as dcp
+    from decode_context_mla_dcp_gb300.inputs import MLA_SCALE
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    out = {}
+    n_calls, B, T = 10, 8, 4096
+    for name, H, cp, n_split in (("deepseek-v2 shard, 128 heads", 128, 8, 2), ("kimi-k2.5 shard, 64 heads", 64, 4, 4)):
+        q = torch.randn((B, H, 576), generator=gen, device="cuda").to(torch.bfloat16)
+        kvs = [torch.randn((B, T, 576), generator=gen, device="cuda").to(torch.bfloat16) for _ in range(n_calls)]
+        lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+        ns = 16
+        po = [torch.empty((B, H, 512), dtype=torch.bfloat16, device="cuda") for _ in range(ns)]
+        pl = [torch.empty((B, H), dtype=torch.float32, device="cuda") for _ in range(ns)]
+
+        def timed(fn):
+            fn(0)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for k in range(n_calls):
+                    fn(k)
+            ts = []
+            for _ in range(10):
+                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                e.record()
+                e.synchronize()
+                ts.append(a.elapsed_time(e) * 1e3 / n_calls)
+            return statistics.median(ts)
+
+        us = timed(lambda k: dcp.mla_decode_partial(q, kvs[k], lens, MLA_SCALE, n_split=ns, outs=po, lses=pl,
+                                                    flags=dcp.DCP_FLAG_PDL))
+        kv_bytes = B * T * 576 * 2
+        nbytes = kv_bytes + B * H * 576 * 2 + ns * B * H * (512 * 2 + 4)
+        flops = 2 * B * H * T * (576 + 512)
+        out[f"producer, {name}"] = {
+            "shape": f"B={B}, H={H}, shard tokens={T}, n_split={ns}", "us_per_call": round(us, 2),
+            "gbs": round(nbytes / us / 1e3, 1), "tflops": round(flops / us / 1e6, 1),
+            "frac_of_measured_hbm": round(nbytes / us / 1e3 / hbm_peak, 4),
+            "frac_of_measured_bf16_tensor": round(flops / us / 1e6 / tensor_peak, 4)}
+        # fused: the same cache split over cp shards of T/cp tokens each
+        Ts = T // cp
+        shard_kvs = [[kvs[k][:, j * Ts:(j + 1) * Ts].contiguous() for j in range(cp)] for k in range(n_calls)]
+        shard_lens = [torch.full((B,), Ts, dtype=torch.int32, device="cuda") for _ in range(cp)]
+        ws = torch.empty((dcp.dcp_mla_decode_workspace_bytes(cp, n_split, B, H),), dtype=torch.uint8, device="cuda")
+        fo = [torch.empty((B, H // cp, 512), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
+        fl = [torch.empty((B, H // cp), dtype=torch.float32, device="cuda") for _ in range(cp)]
+        us_f = timed(lambda k: dcp.mla_decode_dcp(q, shard_kvs[k], shard_lens, MLA_SCALE, n_split=n_split,
+                                                  workspace=ws, outs=fo, lse_outs=fl, flags=dcp.DCP_FLAG_PDL))
+        out[f"fused producer+merge, {name}"] = {
+            "shape": f"B={B}, H={H}, cp={cp} shards x {Ts} tokens, n_split={n_split}", "us_per_call": round(us_f, 2),
+            "kv_gbs": round(kv_bytes / us_f / 1e3, 1), "tflops": round(flops / us_f / 1e6, 1)}
+        del q, kvs, shard_kvs, po, pl, ws, fo, fl
+        torch.cuda.empty_cache()
+    return out
+
+
 def e2e_measure(cfg, steps: int):
     """The same metric end to end through the public API: every step copies
     each row count's inputs from pinned host memory, merges, and reads the
@@ -559,6 +636,7 @@ def run_ours(args):
         del sets, graphs
         torch.cuda.empty_cache()
         out["extras"]["largest_config"] = stress_extra(peak)
+        out["extras"]["dcp_producer_and_fused_decode"] = mla_extras(peak, measured_tensor_peak())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg)
     if rank == 0:
@@ -578,6 +656,20 @@ def run_case(args):
     from decode_context_mla_dcp_gb300.inputs import CONFIGS, make_merge_inputs
     torch.cuda.set_device(dist_env()[2])
     dcp_build.build()
+    if args.case == "mla":
+        # the producer on a DeepSeek-V2-shaped shard: 8 rows x 128 heads x 4096 tokens, 16 splits
+        from decode_context_mla_dcp_gb300.inputs import MLA_SCALE
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(0)
+        B, H, T = 8, 128, 4096
+        q = torch.randn((B, H, 576), generator=gen, device="cuda").to(torch.bfloat16)
+        kvs = [torch.randn((B, T, 576), generator=gen, device="cuda").to(torch.bfloat16) for _ in range(args.calls)]
+        lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+        for kv in kvs:
+            dcp.mla_decode_partial(q, kv, lens, MLA_SCALE, n_split=16)
+        torch.cuda.synchronize()
+        print(f"case mla x {args.calls} calls done", flush=True)
+        return 0
     cfg = CONFIGS[args.case]
     rows_list = [int(r) for r in args.rows.split(",")] if args.rows else list(cfg.rows)
     flags = dcp.DCP_FLAG_PDL
@@ -610,7 +702,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the L2-hot, no-PDL and stress extras")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["kimi", "deepseek", "spec", "stress"],
+    ap.add_argument("--case", choices=["kimi", "deepseek", "spec", "stress", "mla"],
                     help="profiling mode: plain calls of one config, no timing")
     ap.add_argument("--rows", default="", help="with --case: comma-separated row counts")
     ap.add_argument("--calls", type=int, default=3, help="with --case: calls per row count")
