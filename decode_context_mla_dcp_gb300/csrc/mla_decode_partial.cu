@@ -373,12 +373,16 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
 template <int kDk, int kG>
 cudaError_t launch(const Params& prm, int64_t B, int n_slots, unsigned flags, cudaStream_t stream) {
     constexpr int bytes = smem_bytes<kDk, kG>();
-    static bool configured = false;  // the attribute is per kernel; setting it twice is harmless
-    if (!configured) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(mla_partial_kernel<kDk, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    // The shared-memory opt-in is a per-device attribute of the kernel: set it
+    // once per device (setting it again is harmless, so racing callers are fine).
+    static int configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
+        e = cudaFuncSetAttribute(mla_partial_kernel<kDk, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
-        configured = true;
+        if (dev >= 0 && dev < 64) __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)n_slots, (unsigned)(prm.H / (16 * kG)), (unsigned)B);
