@@ -20,6 +20,8 @@
 //     output block of a warp lives in registers.
 //   * at the end: divide by the running sum, round to bf16, and write the
 //     partial output and the LSE (base e or 2).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -36,6 +38,7 @@ constexpr int kDv = 512;
 constexpr int kNt = 32;              // tokens per KV tile
 constexpr int kSPad = 4;             // fp32 padding of a score row in shared memory
 constexpr unsigned kFlagPdl = 1u;
+constexpr unsigned kFlagMmaSync = 2u;   // DCP_MLA_FLAG_MMA_SYNC
 constexpr long long kWaitLimitNs = 2000000000LL;
 
 constexpr int kSlots = 16;            // (shard, split) outputs of one launch
@@ -368,6 +371,364 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
     }
 }
 
+// ---- the tcgen05 kernel -------------------------------------------------------------
+//
+// The same partials on the 5th-generation tensor cores, transposed so that the
+// 128 tokens of a tile sit on the MMA's M (TMEM lanes) and a block of kNH heads
+// on its N (TMEM columns):
+//   S^T[128 x kNH] = K_tile[128 x Dk] . Q^T          (36 MMAs of K = 16 for Dk = 576)
+//   O^T[512 x kNH] += V_tile^T[512 x 128] . P^T      (4 row blocks x 8 MMAs)
+// Q and each KV tile arrive by TMA in 128-byte-swizzled 64-wide slices; the KV
+// slices serve as the K-major A operand of the scores and, read along the
+// latent dims, as the M-major A operand of the values. TMEM holds S^T (kNH
+// columns) and O^T (4 x kNH columns). Thread t of the 128 owns token t: it reads
+// its score row, the per-head maxima over the tile come from a reduce-scatter
+// butterfly across lanes and shared memory, and the running maximum moves only
+// when a head's tile maximum exceeds it by more than 2^8 (then O^T is rescaled
+// in TMEM), so the rescale is rare. P^T (bf16) is written into the RoPE slice's
+// buffer once the scores are done (into its own buffer when Dk = 512).
+
+constexpr int kTcTok = 128;                  // tokens per tile
+constexpr int kTcAtom = kTcTok * 128;        // one 64-wide slice of 128 token rows (bytes)
+constexpr int kTcMiscBytes = 2048;
+
+struct TcParams {
+    CUtensorMap tm_q;                 // Q as [B*H rows, Dk], box [64, kNH], 128B swizzle
+    CUtensorMap tm_kv[kSlots];        // shard caches as [B*T rows, Dk], box [64, 128], 128B swizzle
+    const int* kv_len[kSlots];
+    uint8_t* out[kSlots];
+    float* lse[kSlots];
+    int* status;
+    int64_t T;
+    int H, n_split;
+    float scale_log2;
+    float lse_scale;
+};
+
+template <int kDk, int kNH>
+__host__ __device__ constexpr int tc_smem_bytes() {
+    return (kDk / 64) * kTcAtom + (kDk / 64) * kNH * 128 + (kDk == 576 ? 0 : 2 * kNH * 128) + kTcMiscBytes + 1024;
+}
+
+// byte offset of element (row, col) in a 128-byte-swizzled slice of 128-byte rows
+__device__ __forceinline__ uint32_t sw128(int row, int col) {
+    return (row >> 3) * 1024 + (row & 7) * 128 + ((((col * 2) >> 4) ^ (row & 7)) << 4) + ((col * 2) & 15);
+}
+// shared-memory matrix descriptor: 128-byte swizzle, leading / stride byte offsets
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+// 16 consecutive TMEM columns of this warp's 32 lanes -> 16 registers per thread
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Reduce-scatter across the 32 lanes of a warp: kN values per lane in, the
+// reduction (max or sum) over all lanes out, lane l keeping the results for
+// heads [h0, h0 + max(kN/32, 1)) with h0 = (l / (32 * max(kN/32, 1) / kN)) * max(kN/32, 1).
+template <int kN, int kOff, bool kSum>
+struct WarpReduceScatter {
+    __device__ __forceinline__ static void run(float* v, int lane) {
+        if constexpr (kOff > 0) {
+            if constexpr (kN > 1) {
+                const bool up = (lane & kOff) != 0;
+#pragma unroll
+                for (int j = 0; j < kN / 2; ++j) {
+                    const float send = up ? v[j] : v[j + kN / 2];
+                    const float keep = up ? v[j + kN / 2] : v[j];
+                    const float recv = __shfl_xor_sync(0xffffffffu, send, kOff);
+                    v[j] = kSum ? keep + recv : fmaxf(keep, recv);
+                }
+                WarpReduceScatter<kN / 2, kOff / 2, kSum>::run(v, lane);
+            } else {
+                const float recv = __shfl_xor_sync(0xffffffffu, v[0], kOff);
+                v[0] = kSum ? v[0] + recv : fmaxf(v[0], recv);
+                WarpReduceScatter<1, kOff / 2, kSum>::run(v, lane);
+            }
+        }
+    }
+};
+
+// Per-head reduction over the CTA's 128 token-threads of v[kNH]; results land in
+// out[kNH] in shared memory (red is a [4][kNH] scratch area).
+template <int kNH, bool kSum>
+__device__ __forceinline__ void cta_reduce_heads(float* v, int warp, int lane, float* red, float* out) {
+    constexpr int kFinal = kNH / 32 > 1 ? kNH / 32 : 1;
+    WarpReduceScatter<kNH, 16, kSum>::run(v, lane);
+    const int h0 = (lane / (32 * kFinal / kNH)) * kFinal;
+#pragma unroll
+    for (int e = 0; e < kFinal; ++e) red[warp * kNH + h0 + e] = v[e];
+    __syncthreads();
+    if (threadIdx.x < kNH) {
+        const int h = threadIdx.x;
+        const float a = red[h], b = red[kNH + h], c = red[2 * kNH + h], d = red[3 * kNH + h];
+        out[h] = kSum ? (a + b) + (c + d) : fmaxf(fmaxf(a, b), fmaxf(c, d));
+    }
+    __syncthreads();
+}
+
+template <int kDk, int kNH>
+__global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_constant__ TcParams p) {
+    constexpr int kAtoms = kDk / 64;            // 64-wide slices of a row: 9 (Dk 576) or 8 (Dk 512)
+    constexpr int kQAtom = kNH * 128;           // bytes of one Q slice
+    constexpr bool kPInRope = kAtoms == 9;      // P^T reuses the RoPE slice's buffer
+    constexpr uint32_t kCols = 512;             // TMEM columns: S^T [0, kNH), O^T [kNH, 5 kNH)
+    constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kNH >> 3) << 17) |
+                                 ((uint32_t)(kTcTok >> 4) << 24);  // fp32 += bf16 x bf16, both K-major
+    constexpr uint32_t kIdescO = kIdescS | (1u << 15);             // A read M-major
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* const smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* const kv_s = smem;
+    uint8_t* const q_s = kv_s + kAtoms * kTcAtom;
+    uint8_t* const p_s = kPInRope ? kv_s + 8 * kTcAtom : q_s + kAtoms * kQAtom;
+    uint8_t* const misc = kPInRope ? q_s + kAtoms * kQAtom : p_s + 2 * kQAtom;
+    uint64_t* const bar_q = reinterpret_cast<uint64_t*>(misc);
+    uint64_t* const bar_kv = bar_q + 1;
+    uint64_t* const bar_s = bar_q + 2;
+    uint64_t* const bar_o = bar_q + 3;
+    uint32_t* const tslot = reinterpret_cast<uint32_t*>(bar_q + 4);
+    float* const red = reinterpret_cast<float*>(misc + 64);  // [4][kNH]
+    float* const m_s = red + 4 * kNH;                        // running max per head (base-2 units)
+    float* const a_s = m_s + kNH;                            // this tile's rescale factor per head
+    float* const t_s = a_s + kNH;                            // tile max, then the final sums
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slot = blockIdx.x;
+    const int shard = slot / p.n_split;
+    const int split = slot - shard * p.n_split;
+    const int h0 = blockIdx.y * kNH;
+    const int b = blockIdx.z;
+
+    // set-up that reads no input overlaps the previous kernel
+    if (tid == 0) {
+        mbar_init(bar_q, 1);
+        mbar_init(bar_kv, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_q)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_kv[shard])) : "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "r"(kCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid < kNH) m_s[tid] = -INFINITY;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tlane = (uint32_t)(32 * warp) << 16;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    int64_t len = p.kv_len[shard][b];
+    len = len < 0 ? 0 : (len > p.T ? p.T : len);
+    const int64_t chunk = (len + p.n_split - 1) / p.n_split;
+    const int64_t t_begin = (int64_t)split * chunk;
+    const int64_t t_end = t_begin + chunk < len ? t_begin + chunk : len;
+    const int ntok = t_end > t_begin ? (int)(t_end - t_begin) : 0;
+    uint8_t* const out = p.out[slot];
+    float* const lse = p.lse[slot];
+    const int64_t out_row0 = ((int64_t)b * p.H + h0) * kDv;
+
+    if (ntok == 0) {  // empty range: output 0, LSE -inf
+        for (int i = tid; i < kNH * kDv / 8; i += 128)
+            reinterpret_cast<uint4*>(out + out_row0 * 2)[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (tid < kNH) lse[(int64_t)b * p.H + h0 + tid] = -INFINITY;
+    } else {
+        const int ntiles = (ntok + kTcTok - 1) / kTcTok;
+        const int row0 = (int)((int64_t)b * p.T + t_begin);
+        if (tid == 0) {
+            mbar_expect_tx(bar_q, (uint32_t)(kAtoms * kQAtom));
+            for (int a = 0; a < kAtoms; ++a) tma_load_2d(q_s + a * kQAtom, &p.tm_q, a * 64, b * p.H + h0, bar_q);
+            mbar_expect_tx(bar_kv, (uint32_t)(kAtoms * kTcAtom));
+            for (int a = 0; a < kAtoms; ++a) tma_load_2d(kv_s + a * kTcAtom, &p.tm_kv[shard], a * 64, row0, bar_kv);
+        }
+        float l_part[kNH];  // this token-thread's share of each head's sum
+#pragma unroll
+        for (int h = 0; h < kNH; ++h) l_part[h] = 0.f;
+        mbar_wait(bar_q, 0, p.status);
+
+        for (int i = 0; i < ntiles; ++i) {
+            const uint32_t ph = (uint32_t)(i & 1);
+            mbar_wait(bar_kv, ph, p.status);
+            if (tid == 0) {  // scores: S^T = K_tile . Q^T
+                tc_fence_after();
+#pragma unroll 1
+                for (int a = 0; a < kAtoms; ++a) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc(smem_u32(kv_s + a * kTcAtom) + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc(smem_u32(q_s + a * kQAtom) + kk * 32, 16, 1024);
+                        umma_f16(tmem, ad, bd, kIdescS, (a | kk) != 0);
+                    }
+                }
+                umma_commit(bar_s);
+            }
+            mbar_wait(bar_s, ph, p.status);
+            tc_fence_after();
+
+            float sv[kNH];
+#pragma unroll
+            for (int c = 0; c < kNH; c += 16) tmem_ld16(tmem + tlane + c, sv + c);
+            tmem_wait_ld();
+            const int valid = (ntok - i * kTcTok) < kTcTok ? (ntok - i * kTcTok) : kTcTok;
+            const bool live = tid < valid;
+#pragma unroll
+            for (int h = 0; h < kNH; ++h) sv[h] = live ? sv[h] * p.scale_log2 : -INFINITY;
+            if (!live) {  // a token past the range: its value row must be finite (0 x V)
+#pragma unroll 1
+                for (int a = 0; a < 8; ++a) {
+                    uint4* row = reinterpret_cast<uint4*>(kv_s + a * kTcAtom + (tid >> 3) * 1024 + (tid & 7) * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            // per-head maximum over the tile's tokens
+            {
+                float mx[kNH];
+#pragma unroll
+                for (int h = 0; h < kNH; ++h) mx[h] = sv[h];
+                cta_reduce_heads<kNH, false>(mx, warp, lane, red, t_s);
+            }
+            // move the running max only when some head's tile max exceeds it by more than 2^8
+            const bool need = tid < kNH && t_s[tid] > m_s[tid] + 8.f;
+            const int any = __syncthreads_or(need);
+            if (tid < kNH) {
+                if (any) {
+                    const float mn = fmaxf(m_s[tid], t_s[tid]);
+                    a_s[tid] = ex2(m_s[tid] - mn);
+                    m_s[tid] = mn;
+                } else {
+                    a_s[tid] = 1.f;
+                }
+            }
+            __syncthreads();
+            if (any && i > 0) {  // rescale O^T (the previous tile's value MMAs are done)
+                mbar_wait(bar_o, (uint32_t)((i - 1) & 1), p.status);
+                tc_fence_after();
+#pragma unroll 1
+                for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                    for (int c = 0; c < kNH; c += 16) {
+                        float ov[16];
+                        tmem_ld16(tmem + tlane + kNH + m * kNH + c, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) ov[j] *= a_s[c + j];
+                        tmem_st16(tmem + tlane + kNH + m * kNH + c, ov);
+                    }
+                }
+                tmem_wait_st();
+            }
+            // probabilities, this thread's share of the sums, and P^T (bf16, K-major over tokens)
+            {
+                uint8_t* const prow = p_s + (tid >> 6) * kQAtom;
+                const int tl = tid & 63;
+#pragma unroll
+                for (int h = 0; h < kNH; ++h) {
+                    const float pr = ex2(sv[h] - m_s[h]);
+                    l_part[h] = l_part[h] * a_s[h] + pr;
+                    *reinterpret_cast<__nv_bfloat16*>(prow + sw128(h, tl)) = __float2bfloat16_rn(pr);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {  // values: O^T += V_tile^T . P^T, four 128-row blocks of the 512 latent dims
+                tc_fence_after();
+#pragma unroll 1
+                for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad = smem_desc(smem_u32(kv_s + 2 * m * kTcAtom) + kk * 2048, kTcAtom, 1024);
+                        const uint64_t bd = smem_desc(smem_u32(p_s + (kk >> 2) * kQAtom) + (kk & 3) * 32, 16, 1024);
+                        umma_f16(tmem + kNH + m * kNH, ad, bd, kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                umma_commit(bar_o);
+                if (i + 1 < ntiles) {  // the next tile reuses every buffer once these MMAs are done
+                    mbar_wait(bar_o, ph, p.status);
+                    mbar_expect_tx(bar_kv, (uint32_t)(kAtoms * kTcAtom));
+                    for (int a = 0; a < kAtoms; ++a)
+                        tma_load_2d(kv_s + a * kTcAtom, &p.tm_kv[shard], a * 64, row0 + (i + 1) * kTcTok, bar_kv);
+                }
+            }
+        }
+
+        // final sums, then normalise, round to bf16 and store; LSE = m + log2(l)
+        mbar_wait(bar_o, (uint32_t)((ntiles - 1) & 1), p.status);
+        tc_fence_after();
+        cta_reduce_heads<kNH, true>(l_part, warp, lane, red, t_s);
+#pragma unroll 1
+        for (int m = 0; m < 4; ++m) {
+#pragma unroll
+            for (int c = 0; c < kNH; c += 16) {
+                float ov[16];
+                tmem_ld16(tmem + tlane + kNH + m * kNH + c, ov);
+                tmem_wait_ld();
+                const int dv = 128 * m + 32 * warp + lane;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float v = ov[j] / t_s[c + j];
+                    *reinterpret_cast<__nv_bfloat16*>(out + (out_row0 + (int64_t)(c + j) * kDv + dv) * 2) =
+                        __float2bfloat16_rn(v);
+                }
+            }
+        }
+        if (tid < kNH) lse[(int64_t)b * p.H + h0 + tid] = (m_s[tid] + log2f(t_s[tid])) * p.lse_scale;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+}
+
 // ---- host side -----------------------------------------------------------------
 
 template <int kDk, int kG>
@@ -406,6 +767,67 @@ cudaError_t launch_dk(const Params& prm, int64_t B, int n_slots, unsigned flags,
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// cuTensorMapEncodeTiled, from the driver through the runtime (no link to libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            (void)cudaGetLastError();
+            f = nullptr;
+        }
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// A [rows, Dk] bf16 matrix read in [box_rows, 64] boxes with 128-byte swizzle.
+bool encode_rows(CUtensorMap* tm, const void* base, int Dk, uint64_t rows, uint32_t box_rows) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)Dk, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)Dk * 2};
+    cuuint32_t box[2] = {64u, box_rows};
+    cuuint32_t estride[2] = {1u, 1u};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int kDk, int kNH>
+cudaError_t launch_tc(const TcParams& prm, int64_t B, int n_slots, unsigned flags, cudaStream_t stream) {
+    constexpr int bytes = tc_smem_bytes<kDk, kNH>();
+    static int configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
+        e = cudaFuncSetAttribute(mla_partial_tc_kernel<kDk, kNH>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n_slots, (unsigned)(prm.H / kNH), (unsigned)B);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (flags & kFlagPdl) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel<kDk, kNH>, prm);
+}
+
+template <int kDk>
+cudaError_t launch_tc_dk(const TcParams& prm, int64_t B, int n_slots, unsigned flags, cudaStream_t stream) {
+    if (prm.H % 64 == 0) return launch_tc<kDk, 64>(prm, B, n_slots, flags, stream);
+    if (prm.H % 32 == 0) return launch_tc<kDk, 32>(prm, B, n_slots, flags, stream);
+    return launch_tc<kDk, 16>(prm, B, n_slots, flags, stream);
+}
+
 }  // namespace
 
 extern "C" int dcp_mla_decode_smem_bytes(int Dk, int H) {
@@ -428,7 +850,7 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
         return DCP_MLA_ERR_BAD_SHAPE;
     if (n_split < 1 || n_split > DCP_MLA_SPLIT_MAX) return DCP_MLA_ERR_BAD_SPLIT;
     if (n_shard < 1 || n_shard * n_split > kSlots) return DCP_MLA_ERR_BAD_CP;
-    if ((flags & ~kFlagPdl) != 0) return DCP_MLA_ERR_BAD_FLAGS;
+    if ((flags & ~(kFlagPdl | kFlagMmaSync)) != 0) return DCP_MLA_ERR_BAD_FLAGS;
     if (!aligned(q, 16) || (status != nullptr && !aligned(status, 4))) return DCP_MLA_ERR_MISALIGNED;
     Params prm;
     for (int k = 0; k < kSlots; ++k) {
@@ -451,6 +873,37 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
         prm.lse[k] = lse_ptrs[k];
     }
     if (B == 0) return 0;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!(flags & kFlagMmaSync)) {  // the tcgen05 kernel
+        TcParams tp;
+        const int nh = H % 64 == 0 ? 64 : (H % 32 == 0 ? 32 : 16);
+        if (!encode_rows(&tp.tm_q, q, Dk, (uint64_t)B * H, (uint32_t)nh)) return DCP_MLA_ERR_TENSOR_MAP;
+        const uint64_t kv_rows = (uint64_t)B * (uint64_t)T > 0 ? (uint64_t)B * (uint64_t)T : 1;
+        if (kv_rows > 0x7fffffffull) return DCP_MLA_ERR_BAD_SHAPE;
+        for (int j = 0; j < kSlots; ++j) {
+            tp.kv_len[j] = prm.kv_len[j];
+            tp.out[j] = prm.out[j];
+            tp.lse[j] = prm.lse[j];
+            if (j < n_shard) {
+                if (!encode_rows(&tp.tm_kv[j], kv_ptrs[j], Dk, kv_rows, (uint32_t)kTcTok)) return DCP_MLA_ERR_TENSOR_MAP;
+            } else {
+                tp.tm_kv[j] = tp.tm_q;
+            }
+        }
+        tp.status = status;
+        tp.T = T;
+        tp.H = H;
+        tp.n_split = n_split;
+        tp.scale_log2 = scale * 1.4426950408889634f;
+        tp.lse_scale = lse_base_e ? 0.6931471805599453f : 1.0f;
+        const cudaError_t e = Dk == 576 ? launch_tc_dk<576>(tp, B, n_slots, flags, st)
+                                        : launch_tc_dk<512>(tp, B, n_slots, flags, st);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return (int)e;
+        }
+        return 0;
+    }
     prm.q = static_cast<const uint8_t*>(q);
     prm.status = status;
     prm.T = T;
@@ -458,9 +911,8 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
     prm.n_split = n_split;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.lse_scale = lse_base_e ? 0.6931471805599453f : 1.0f;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = Dk == 576 ? launch_dk<576>(prm, B, n_slots, flags, st)
-                                    : launch_dk<512>(prm, B, n_slots, flags, st);
+    const cudaError_t e = Dk == 576 ? launch_dk<576>(prm, B, n_slots, flags & kFlagPdl, st)
+                                    : launch_dk<512>(prm, B, n_slots, flags & kFlagPdl, st);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return (int)e;
@@ -537,7 +989,7 @@ extern "C" int dcp_mla_decode(const void* q, const void* const* kv_ptrs, const i
     lay.dst_head = Dv;
     lay.lse_out_row = Hl;
     return dcp_lse_reduce_ex(part_out, part_lse, n_src, B, H, Dv, lse_base_e, DCP_DTYPE_BF16, dst, lout, &lay, nullptr,
-                             1, flags & DCP_FLAG_PDL, stream);
+                             1, flags & kFlagPdl, stream);
 }
 
 // ---- the no-allocation variant -----------------------------------------------------

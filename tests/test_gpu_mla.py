@@ -76,15 +76,20 @@ def oracle_partials(q_bits, kv_bits, lens, n_split, scale, base_e, dv=512):
     return outs, lses
 
 
+KERNELS = [0, dcp.DCP_MLA_FLAG_MMA_SYNC]  # tcgen05 (default), warp-level mma.sync
+
+
+@pytest.mark.parametrize("kflags", KERNELS)
 @pytest.mark.parametrize("H,Dk,T,n_split", [(16, 576, 100, 1), (64, 576, 257, 3), (128, 576, 96, 2),
-                                            (32, 512, 64, 1), (16, 512, 33, 16)])
+                                            (32, 512, 64, 1), (16, 512, 33, 16), (64, 576, 700, 2),
+                                            (64, 512, 300, 1)])
 @pytest.mark.parametrize("base_e", [True, False])
-def test_partials_match_oracle(oracle_mod, H, Dk, T, n_split, base_e):
+def test_partials_match_oracle(oracle_mod, H, Dk, T, n_split, base_e, kflags):
     B = 4
     q, kv = make_mla_inputs(B, H, T, Dk, seed=H + T)
     lens = np.array([T, 1, 0, T - 5 if T > 5 else T], dtype=np.int32)
     outs, lses = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), torch.from_numpy(lens).cuda(), MLA_SCALE,
-                                        lse_base_e=base_e, n_split=n_split)
+                                        lse_base_e=base_e, n_split=n_split, flags=kflags)
     torch.cuda.synchronize()
     ref_o, ref_l = oracle_partials(q, kv, lens, n_split, MLA_SCALE, base_e)
     for s in range(n_split):
@@ -224,14 +229,15 @@ def _interleaved_shards(kv_full, L, cp):
     return kvs, lens
 
 
+@pytest.mark.parametrize("kflags", KERNELS)
 @pytest.mark.parametrize("cp,n_split,H,Dk", [(4, 2, 64, 576), (8, 2, 128, 576), (2, 4, 16, 512), (1, 16, 16, 576)])
-def test_fused_dcp_decode_equals_full_attention(oracle_mod, cp, n_split, H, Dk):
+def test_fused_dcp_decode_equals_full_attention(oracle_mod, cp, n_split, H, Dk, kflags):
     from oracle.attention import attention
     B, L_max = 3, 260
     q, kv_full = make_mla_inputs(B, H, L_max, Dk, seed=cp * 100 + n_split)
     L = np.array([L_max, 41, max(cp - 1, 1)], dtype=np.int32)
     kvs, lens = _interleaved_shards(kv_full, L, cp)
-    outs, louts = dcp.mla_decode_dcp(dev_bf16(q), kvs, lens, MLA_SCALE, n_split=n_split)
+    outs, louts = dcp.mla_decode_dcp(dev_bf16(q), kvs, lens, MLA_SCALE, n_split=n_split, flags=kflags)
     torch.cuda.synchronize()
     Hl = H // cp
     for b in range(B):
@@ -269,3 +275,27 @@ def test_fused_dcp_decode_graph_replay_and_workspace_reuse():
     assert all(torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
                for a, b in zip(ref, got))
+
+
+@pytest.mark.parametrize("H", [16, 64, 128])
+def test_tcgen05_and_mma_sync_kernels_agree(H):
+    """Long ranges (many 128-token tiles, running-max moves) on both kernels."""
+    B, T = 2, 2000
+    q, kv = make_mla_inputs(B, H, T, 576, seed=H)
+    # a drifting key scale makes later tiles' maxima exceed earlier ones (rescale path)
+    kvf = widen(kv) * np.linspace(0.5, 1.5, T)[None, :, None]
+    kv = bf16_bits(kvf.astype(np.float32))
+    lens = torch.tensor([T, 1500], dtype=torch.int32, device="cuda")
+    a_o, a_l = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), lens, MLA_SCALE, n_split=2)
+    b_o, b_l = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), lens, MLA_SCALE, n_split=2,
+                                      flags=dcp.DCP_MLA_FLAG_MMA_SYNC)
+    torch.cuda.synchronize()
+    from oracle.attention import attention
+    for s in range(2):
+        for b, L in enumerate([T, 1500]):
+            chunk = -(-L // 2)
+            t0, t1 = s * chunk, min(L, (s + 1) * chunk)
+            o_ref, l_ref = attention(widen(q[b:b + 1]), widen(kv[b, t0:t1]), MLA_SCALE, dv=512)
+            check_out(a_o[s][b:b + 1], o_ref, f"tcgen05 split {s} row {b}")
+            check_out(b_o[s][b:b + 1], o_ref, f"mma.sync split {s} row {b}")
+            check_lse(a_l[s][b:b + 1], l_ref, f"tcgen05 split {s} row {b}")
