@@ -364,11 +364,12 @@ def mla_extras(hbm_peak, tensor_peak):
     gen.manual_seed(0)
     out = {}
     n_calls, B, T = 10, 8, 4096
-    for name, H, cp, n_split in (("deepseek-v2 shard, 128 heads", 128, 8, 2), ("kimi-k2.5 shard, 64 heads", 64, 4, 4)):
+    # split counts chosen so that one launch is about one wave of one-CTA-per-SM blocks
+    for name, H, cp, n_split, ns in (("deepseek-v2 shard, 128 heads", 128, 8, 2, 9),
+                                     ("kimi-k2.5 shard, 64 heads", 64, 4, 4, 16)):
         q = torch.randn((B, H, 576), generator=gen, device="cuda").to(torch.bfloat16)
         kvs = [torch.randn((B, T, 576), generator=gen, device="cuda").to(torch.bfloat16) for _ in range(n_calls)]
         lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
-        ns = 16
         po = [torch.empty((B, H, 512), dtype=torch.bfloat16, device="cuda") for _ in range(ns)]
         pl = [torch.empty((B, H), dtype=torch.float32, device="cuda") for _ in range(ns)]
 
@@ -391,6 +392,8 @@ def mla_extras(hbm_peak, tensor_peak):
 
         us = timed(lambda k: dcp.mla_decode_partial(q, kvs[k], lens, MLA_SCALE, n_split=ns, outs=po, lses=pl,
                                                     flags=dcp.DCP_FLAG_PDL))
+        us_mma = timed(lambda k: dcp.mla_decode_partial(q, kvs[k], lens, MLA_SCALE, n_split=ns, outs=po, lses=pl,
+                                                        flags=dcp.DCP_FLAG_PDL | dcp.DCP_MLA_FLAG_MMA_SYNC))
         kv_bytes = B * T * 576 * 2
         nbytes = kv_bytes + B * H * 576 * 2 + ns * B * H * (512 * 2 + 4)
         flops = 2 * B * H * T * (576 + 512)
@@ -398,7 +401,8 @@ def mla_extras(hbm_peak, tensor_peak):
             "shape": f"B={B}, H={H}, shard tokens={T}, n_split={ns}", "us_per_call": round(us, 2),
             "gbs": round(nbytes / us / 1e3, 1), "tflops": round(flops / us / 1e6, 1),
             "frac_of_measured_hbm": round(nbytes / us / 1e3 / hbm_peak, 4),
-            "frac_of_measured_bf16_tensor": round(flops / us / 1e6 / tensor_peak, 4)}
+            "frac_of_measured_bf16_tensor": round(flops / us / 1e6 / tensor_peak, 4),
+            "kernel": "tcgen05", "mma_sync_kernel_us_per_call": round(us_mma, 2)}
         # fused: the same cache split over cp shards of T/cp tokens each
         Ts = T // cp
         shard_kvs = [[kvs[k][:, j * Ts:(j + 1) * Ts].contiguous() for j in range(cp)] for k in range(n_calls)]

@@ -28,11 +28,12 @@ EXPORTED_SYMBOLS = ("dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strer
 DCP_MLA_NOALLOC_SCRATCH_BYTES = 32 << 20
 DCP_MLA_SPLIT_MAX = 16
 DCP_MLA_FLAG_MMA_SYNC = 2
+DCP_MLA_FLAG_TCGEN05 = 4
 _MLA_ERRORS = {-101: "q, kv, kv_len, out_ptrs, lse_ptrs or an entry is NULL",
                -102: "B must be in [0, 65535], T >= 0, H a positive multiple of 16, Dk 512 or 576, Dv 512",
                -103: "n_split must be in [1, 16]",
                -104: "q, kv and outputs must be 16-byte aligned; LSE, kv_len and status 4-byte aligned",
-               -105: "only DCP_FLAG_PDL and DCP_MLA_FLAG_MMA_SYNC are accepted",
+               -105: "unknown flag bits, or DCP_MLA_FLAG_MMA_SYNC together with DCP_MLA_FLAG_TCGEN05",
                -106: "workspace is NULL, not 256-byte aligned, or smaller than dcp_mla_decode_workspace_bytes",
                -107: "cp*n_split must be <= 16 and divide H",
                -108: "the partials need more than the built-in 32 MiB scratch (DCP_MLA_NOALLOC_SCRATCH_BYTES)",

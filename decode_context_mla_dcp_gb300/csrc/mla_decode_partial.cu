@@ -39,6 +39,10 @@ constexpr int kNt = 32;              // tokens per KV tile
 constexpr int kSPad = 4;             // fp32 padding of a score row in shared memory
 constexpr unsigned kFlagPdl = 1u;
 constexpr unsigned kFlagMmaSync = 2u;   // DCP_MLA_FLAG_MMA_SYNC
+constexpr unsigned kFlagTcgen05 = 4u;   // DCP_MLA_FLAG_TCGEN05
+// Below this many tokens per (row, split) the tcgen05 kernel's per-CTA set-up
+// (TMEM, a 72 KB Q load, one 224 KB CTA per SM) outweighs its faster tiles.
+constexpr int64_t kTcMinTokensPerSplit = 256;
 constexpr long long kWaitLimitNs = 2000000000LL;
 
 constexpr int kSlots = 16;            // (shard, split) outputs of one launch
@@ -850,7 +854,8 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
         return DCP_MLA_ERR_BAD_SHAPE;
     if (n_split < 1 || n_split > DCP_MLA_SPLIT_MAX) return DCP_MLA_ERR_BAD_SPLIT;
     if (n_shard < 1 || n_shard * n_split > kSlots) return DCP_MLA_ERR_BAD_CP;
-    if ((flags & ~(kFlagPdl | kFlagMmaSync)) != 0) return DCP_MLA_ERR_BAD_FLAGS;
+    if ((flags & ~(kFlagPdl | kFlagMmaSync | kFlagTcgen05)) != 0) return DCP_MLA_ERR_BAD_FLAGS;
+    if ((flags & kFlagMmaSync) && (flags & kFlagTcgen05)) return DCP_MLA_ERR_BAD_FLAGS;
     if (!aligned(q, 16) || (status != nullptr && !aligned(status, 4))) return DCP_MLA_ERR_MISALIGNED;
     Params prm;
     for (int k = 0; k < kSlots; ++k) {
@@ -874,7 +879,9 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
     }
     if (B == 0) return 0;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (!(flags & kFlagMmaSync)) {  // the tcgen05 kernel
+    const bool use_tc = (flags & kFlagTcgen05) != 0 ||
+                        (!(flags & kFlagMmaSync) && (T + n_split - 1) / n_split >= kTcMinTokensPerSplit);
+    if (use_tc) {  // the tcgen05 kernel
         TcParams tp;
         const int nh = H % 64 == 0 ? 64 : (H % 32 == 0 ? 32 : 16);
         if (!encode_rows(&tp.tm_q, q, Dk, (uint64_t)B * H, (uint32_t)nh)) return DCP_MLA_ERR_TENSOR_MAP;
@@ -896,8 +903,8 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
         tp.n_split = n_split;
         tp.scale_log2 = scale * 1.4426950408889634f;
         tp.lse_scale = lse_base_e ? 0.6931471805599453f : 1.0f;
-        const cudaError_t e = Dk == 576 ? launch_tc_dk<576>(tp, B, n_slots, flags, st)
-                                        : launch_tc_dk<512>(tp, B, n_slots, flags, st);
+        const cudaError_t e = Dk == 576 ? launch_tc_dk<576>(tp, B, n_slots, flags & kFlagPdl, st)
+                                        : launch_tc_dk<512>(tp, B, n_slots, flags & kFlagPdl, st);
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             return (int)e;

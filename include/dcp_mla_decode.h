@@ -30,10 +30,10 @@
  * Numerics. bf16 inputs, fp32 scores and accumulation (tensor-core MMA),
  * softmax in base 2 with the running maximum taken out, probabilities rounded
  * to bf16 for the value product, output rounded to bf16 (round to nearest
- * even), LSE fp32 in the requested base. The default kernel runs on the
- * 5th-generation tensor cores (tcgen05 MMA into TMEM, operands loaded by TMA);
- * DCP_MLA_FLAG_MMA_SYNC selects a warp-level mma.sync kernel instead. The two
- * agree within the stated tolerances, not bit for bit.
+ * even), LSE fp32 in the requested base. Two kernels compute it: one on the
+ * 5th-generation tensor cores (tcgen05 MMA into TMEM, operands loaded by TMA)
+ * and one on warp-level mma.sync (see DCP_MLA_FLAG_*); they agree within the
+ * stated tolerances, not bit for bit.
  *
  * Layout (all contiguous, device memory, caller-owned):
  *   q        [B, H, Dk] bf16, 16-byte aligned
@@ -68,7 +68,7 @@ enum {
     DCP_MLA_ERR_BAD_SPLIT = -103,    /* n_split outside [1, DCP_MLA_SPLIT_MAX] */
     DCP_MLA_ERR_MISALIGNED = -104,   /* q, kv or an output not 16-byte aligned, or an LSE or kv_len
                                         pointer not 4-byte aligned */
-    DCP_MLA_ERR_BAD_FLAGS = -105,    /* flag bits other than DCP_FLAG_PDL (1) and DCP_MLA_FLAG_MMA_SYNC (2) */
+    DCP_MLA_ERR_BAD_FLAGS = -105,    /* unknown flag bits, or both DCP_MLA_FLAG_MMA_SYNC and DCP_MLA_FLAG_TCGEN05 */
     DCP_MLA_ERR_WORKSPACE = -106,    /* workspace NULL, not 256-byte aligned, or smaller than
                                         dcp_mla_decode_workspace_bytes(...) */
     DCP_MLA_ERR_BAD_CP = -107,       /* cp < 1, cp*n_split > 16, or H not a multiple of cp*n_split */
@@ -79,9 +79,15 @@ enum {
     DCP_MLA_ERR_TENSOR_MAP = -110     /* a TMA tensor map for q or a cache could not be encoded */
 };
 
-/* Flags of the producer and the fused decode (besides DCP_FLAG_PDL = 1). */
-#define DCP_MLA_FLAG_MMA_SYNC 2u  /* run the warp-level mma.sync kernel instead of the default
-                                     tcgen05 (TMEM, TMA) kernel; both compute the same partials */
+/*
+ * Flags of the producer and the fused decode (besides DCP_FLAG_PDL = 1). By
+ * default the producer runs the tcgen05 kernel (TMEM accumulators, TMA loads)
+ * when a split holds at least 256 tokens of the cache (ceil(T / n_split) >=
+ * 256) and the warp-level mma.sync kernel otherwise; these flags force one.
+ * Both compute the same partials within the stated tolerances.
+ */
+#define DCP_MLA_FLAG_MMA_SYNC 2u
+#define DCP_MLA_FLAG_TCGEN05 4u
 
 int dcp_mla_decode_partial(const void* q, const void* kv, const int32_t* kv_len,
                            int64_t B, int H, int Dk, int Dv, int64_t T, float scale, int lse_base_e,

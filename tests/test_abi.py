@@ -128,7 +128,7 @@ def test_mla_producer_rejects_bad_arguments(lib):
     assert call(Dk=640) == -102 and call(Dv=256) == -102 and call(T=-1) == -102
     assert call(n_split=0) == -103 and call(n_split=17) == -103
     assert call(q=FAKE + 8) == -104 and call(kv_len=FAKE + 2) == -104 and call(o=arr(FAKE + 4, FAKE)) == -104
-    assert call(flags=4) == -105
+    assert call(flags=8) == -105 and call(flags=6) == -105
     assert call(B=0) == 0  # nothing to do, nothing launched
     assert dcp.dcp_mla_decode_smem_bytes(576, 64) > 150000
     assert "n_split" in dcp.dcp_lse_reduce_strerror(-103)

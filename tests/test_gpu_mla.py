@@ -76,7 +76,7 @@ def oracle_partials(q_bits, kv_bits, lens, n_split, scale, base_e, dv=512):
     return outs, lses
 
 
-KERNELS = [0, dcp.DCP_MLA_FLAG_MMA_SYNC]  # tcgen05 (default), warp-level mma.sync
+KERNELS = [dcp.DCP_MLA_FLAG_TCGEN05, dcp.DCP_MLA_FLAG_MMA_SYNC]
 
 
 @pytest.mark.parametrize("kflags", KERNELS)
@@ -286,7 +286,8 @@ def test_tcgen05_and_mma_sync_kernels_agree(H):
     kvf = widen(kv) * np.linspace(0.5, 1.5, T)[None, :, None]
     kv = bf16_bits(kvf.astype(np.float32))
     lens = torch.tensor([T, 1500], dtype=torch.int32, device="cuda")
-    a_o, a_l = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), lens, MLA_SCALE, n_split=2)
+    a_o, a_l = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), lens, MLA_SCALE, n_split=2,
+                                      flags=dcp.DCP_MLA_FLAG_TCGEN05)
     b_o, b_l = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), lens, MLA_SCALE, n_split=2,
                                       flags=dcp.DCP_MLA_FLAG_MMA_SYNC)
     torch.cuda.synchronize()
