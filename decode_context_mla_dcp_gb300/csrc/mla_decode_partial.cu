@@ -671,15 +671,34 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
                 tmem_wait_st();
             }
             // probabilities, this thread's share of the sums, and P^T (bf16, K-major over tokens)
+            // (the shared reads all come before the stores, so none waits behind one)
             {
+#pragma unroll
+                for (int h = 0; h < kNH; h += 4) {
+                    const float4 mv = *reinterpret_cast<const float4*>(m_s + h);
+                    sv[h] = ex2(sv[h] - mv.x);
+                    sv[h + 1] = ex2(sv[h + 1] - mv.y);
+                    sv[h + 2] = ex2(sv[h + 2] - mv.z);
+                    sv[h + 3] = ex2(sv[h + 3] - mv.w);
+                }
+                if (any) {
+#pragma unroll
+                    for (int h = 0; h < kNH; h += 4) {
+                        const float4 av = *reinterpret_cast<const float4*>(a_s + h);
+                        l_part[h] = l_part[h] * av.x + sv[h];
+                        l_part[h + 1] = l_part[h + 1] * av.y + sv[h + 1];
+                        l_part[h + 2] = l_part[h + 2] * av.z + sv[h + 2];
+                        l_part[h + 3] = l_part[h + 3] * av.w + sv[h + 3];
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < kNH; ++h) l_part[h] += sv[h];
+                }
                 uint8_t* const prow = p_s + (tid >> 6) * kQAtom;
                 const int tl = tid & 63;
 #pragma unroll
-                for (int h = 0; h < kNH; ++h) {
-                    const float pr = ex2(sv[h] - m_s[h]);
-                    l_part[h] = l_part[h] * a_s[h] + pr;
-                    *reinterpret_cast<__nv_bfloat16*>(prow + sw128(h, tl)) = __float2bfloat16_rn(pr);
-                }
+                for (int h = 0; h < kNH; ++h)
+                    *reinterpret_cast<__nv_bfloat16*>(prow + sw128(h, tl)) = __float2bfloat16_rn(sv[h]);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
@@ -709,6 +728,10 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
         mbar_wait(bar_o, (uint32_t)((ntiles - 1) & 1), p.status);
         tc_fence_after();
         cta_reduce_heads<kNH, true>(l_part, warp, lane, red, t_s);
+        // The [kNH, 512] output tile is assembled in the KV buffer (free now:
+        // every MMA is done and no load is pending), then leaves in one bulk
+        // copy: rows h0 .. h0+kNH-1 of out[b] are contiguous.
+        __nv_bfloat16* const o_s = reinterpret_cast<__nv_bfloat16*>(kv_s);
 #pragma unroll 1
         for (int m = 0; m < 4; ++m) {
 #pragma unroll
@@ -718,14 +741,19 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
                 tmem_wait_ld();
                 const int dv = 128 * m + 32 * warp + lane;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float v = ov[j] / t_s[c + j];
-                    *reinterpret_cast<__nv_bfloat16*>(out + (out_row0 + (int64_t)(c + j) * kDv + dv) * 2) =
-                        __float2bfloat16_rn(v);
-                }
+                for (int j = 0; j < 16; ++j) o_s[(c + j) * kDv + dv] = __float2bfloat16_rn(ov[j] / t_s[c + j]);
             }
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (tid == 0) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(out + out_row0 * 2),
+                         "r"(smem_u32(o_s)), "r"((uint32_t)(kNH * kDv * 2))
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
         if (tid < kNH) lse[(int64_t)b * p.H + h0 + tid] = (m_s[tid] + log2f(t_s[tid])) * p.lse_scale;
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the copy has landed
     }
     tc_fence_before();
     __syncthreads();
