@@ -300,3 +300,34 @@ def test_tcgen05_and_mma_sync_kernels_agree(H):
             check_out(a_o[s][b:b + 1], o_ref, f"tcgen05 split {s} row {b}")
             check_out(b_o[s][b:b + 1], o_ref, f"mma.sync split {s} row {b}")
             check_lse(a_l[s][b:b + 1], l_ref, f"tcgen05 split {s} row {b}")
+
+
+@pytest.mark.parametrize("kflags", KERNELS)
+@pytest.mark.parametrize("H,Dk", [(64, 576), (16, 512), (128, 576)])
+def test_running_max_jumps_rescale_the_output(oracle_mod, H, Dk, kflags):
+    """Single cached rows scaled up in later tiles: each spike lifts some heads'
+    maxima by far more than 2^8 (base 2) above the running one, so the output
+    accumulated so far must be rescaled (the lazy-rescale path of the tcgen05
+    kernel, the per-tile rescale of the mma.sync kernel).
+
+    Spikes are single tokens on purpose. A block of many scaled rows averages
+    values of magnitude ~10-40 that cancel to ~0. There the 2^-9 relative
+    rounding of each bf16 probability exceeds the absolute tolerance, and the
+    two kernels agree bit for bit, so such a block tests the probability
+    precision rather than the kernels."""
+    B, T = 2, 1800
+    q, kv = make_mla_inputs(B, H, T, Dk, seed=7 + H)
+    kvf = widen(kv)
+    for t, f in [(300, 4.0), (900, 8.0), (1700, 16.0)]:
+        kvf[0, t] *= f
+    for t, f in [(200, 6.0), (1000, 12.0)]:
+        kvf[1, t] *= f
+    kv = bf16_bits(kvf.astype(np.float32))
+    lens = np.array([T, 1500], dtype=np.int32)
+    for base_e in (True, False):
+        outs, lses = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), torch.from_numpy(lens).cuda(), MLA_SCALE,
+                                            lse_base_e=base_e, n_split=1, flags=kflags)
+        torch.cuda.synchronize()
+        ref_o, ref_l = oracle_partials(q, kv, lens, 1, MLA_SCALE, base_e)
+        check_out(outs[0], ref_o[0], f"H={H} base_e={base_e}")
+        check_lse(lses[0], ref_l[0], f"H={H} base_e={base_e}")
