@@ -257,7 +257,7 @@ class RowSet:
         self.lse = []
         for j in range(cp):
             s = torch.from_numpy(self.inp.srcs[j].view(np.int16)).view(torch.bfloat16).cuda()
-            l = torch.from_numpy(self.inp.lses[j]).cuda()
+            l = torch.from_numpy(np.ascontiguousarray(self.inp.lses[j]).reshape(rows, H)).cuda()  # [B,H,1] -> [B,H]
             self.src.append(s.unsqueeze(0).repeat(slots, 1, 1, 1).contiguous())
             self.lse.append(l.unsqueeze(0).repeat(slots, 1, 1).contiguous())
         self.dst = [torch.empty((slots, rows, Hl, D), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
@@ -306,6 +306,44 @@ def time_graphs(graphs, reps: int, flush=None):
             b.synchronize()
             times.append(a.elapsed_time(b) * 1e3 / CALLS_PER_GRAPH)
         out[key] = statistics.median(times)
+    return out
+
+
+def configs_extra(peak, flush):
+    """The other merge workloads, timed like the sweep (cold L2, PDL, 60
+    calls per graph, each on its own buffers where they fit): the DeepSeek-V2
+    sweep (cp=8, 128 heads, base-e [B, H, 1] LSE) and the speculative-decode
+    batch (1024 rows, 10% empty shards). For the latter the fraction of peak
+    uses the skip-aware bytes (empty shards' payloads are never read)."""
+    import torch
+    import decode_context_mla_dcp_gb300 as dcp
+    from decode_context_mla_dcp_gb300.inputs import CONFIGS
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or (126 << 20)
+    out = {}
+    for name in ("deepseek", "spec"):
+        cfg = CONFIGS[name]
+        res = {}
+        for rows in cfg.rows:
+            nbytes = dcp.algorithmic_bytes(cfg.cp, rows, cfg.H, cfg.D)
+            slots = max(2, min(CALLS_PER_GRAPH, -(-4 * l2 // nbytes)))
+            rs = RowSet(cfg, rows, slots)
+            g = rs.capture(dcp.DCP_FLAG_PDL)
+            us = time_graphs({rows: g}, reps=10, flush=flush)[rows]
+            entry = {"us_per_call": round(us, 3), "bytes_per_call": nbytes,
+                     "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "frac_of_measured_peak": round(nbytes / (us * 1e-6) / 1e9 / peak, 4)}
+            if rs.inp.empty is not None:
+                skipped = int(rs.inp.empty.sum()) * cfg.H  # (row, head, source) payload rows never read
+                skip_bytes = dcp.algorithmic_bytes(cfg.cp, rows, cfg.H, cfg.D, skipped_payload_rows=skipped)
+                entry["empty_row_shards"] = int(rs.inp.empty.sum())
+                entry["skip_aware_bytes_per_call"] = skip_bytes
+                entry["skip_aware_gbs"] = round(skip_bytes / (us * 1e-6) / 1e9, 1)
+                entry["frac_of_measured_peak"] = round(skip_bytes / (us * 1e-6) / 1e9 / peak, 4)
+            res[str(rows)] = entry
+            del g, rs
+            torch.cuda.empty_cache()
+        out[f"{cfg.name} (cp={cfg.cp}, H={cfg.H}, D={cfg.D})"] = res
     return out
 
 
@@ -699,6 +737,7 @@ def run_ours(args):
     if rank == 0 and not args.no_extras:
         del sets, graphs
         torch.cuda.empty_cache()
+        out["extras"]["other_configs_cold_pdl"] = configs_extra(peak, flush)
         out["extras"]["largest_config"] = stress_extra(peak)
         out["extras"]["dcp_producer_and_fused_decode"] = mla_extras(peak, measured_tensor_peak())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
