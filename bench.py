@@ -547,7 +547,39 @@ def cpu_baseline(cfg, budget_s: float = 12.0):
            "sample": f"{passes} passes over the rows {list(cfg.rows)} sweep ({per_pass} algorithmic bytes each), "
                      f"{el:.1f} s, single-threaded fp64 C"}
     out["all_cores"] = cpu_baseline_all_cores(cfg, budget_s / 2)
+    out["parity_vs_oracle"] = sweep_parity(cfg, inputs)
     return out
+
+
+def sweep_parity(cfg, inputs):
+    """The timed path (dcp_lse_reduce_ex with PDL) on the sweep's inputs
+    against the oracle: outputs within |gpu - ref| <= 1e-2 + 8e-3 |ref|,
+    merged LSEs within 1e-5 * max(|ref|, 1)."""
+    import torch
+    import oracle
+    import decode_context_mla_dcp_gb300 as dcp
+    worst_out = worst_lse = 0.0
+    ok = True
+    for inp in inputs:
+        srcs = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda() for x in inp.srcs]
+        lses = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in inp.lses]
+        got_o, got_l = dcp.merge(srcs, lses, inp.lse_base_e, flags=dcp.DCP_FLAG_PDL)
+        torch.cuda.synchronize()
+        ref_o, ref_l = oracle.merge(inp.srcs, inp.lses, inp.lse_base_e)
+        for go, gl, ro, rl in zip(got_o, got_l, ref_o, ref_l):
+            go = go.float().double().cpu().numpy()
+            gl = gl.double().cpu().numpy()
+            err = np.abs(go - ro)
+            ok &= bool((err <= 1e-2 + 8e-3 * np.abs(ro)).all())
+            worst_out = max(worst_out, float(err.max()))
+            fin = np.isfinite(rl)
+            ok &= bool(np.array_equal(np.isfinite(gl), fin))
+            lerr = np.abs(gl[fin] - rl[fin]) / np.maximum(np.abs(rl[fin]), 1.0)
+            if lerr.size:
+                ok &= bool((lerr <= 1e-5).all())
+                worst_lse = max(worst_lse, float(lerr.max()))
+    return {"ok": ok, "rows": [int(i.B) for i in inputs], "max_abs_err_out": worst_out,
+            "max_rel_err_lse": worst_lse}
 
 
 def _oracle_worker(args):
