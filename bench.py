@@ -492,38 +492,64 @@ def e2e_measure(cfg, steps: int):
     hv = host_in.numpy()
     for o, b in arrays:
         hv[o:o + b.size] = b
-    dev_in = torch.empty(off_in, dtype=torch.uint8, device="cuda")
-    dev_out = torch.empty(off_out, dtype=torch.uint8, device="cuda")
-    host_out = torch.empty(off_out, dtype=torch.uint8).pin_memory()
-    calls = []
-    for rows, ins, outs in plan:
-        srcs = [dev_in[o:o + n].view(torch.bfloat16).view(rows, cfg.H, cfg.D) for o, n in ins[:cfg.cp]]
-        lses = [dev_in[o:o + n].view(torch.float32).view(rows, cfg.H) for o, n in ins[cfg.cp:]]
-        dsts = [dev_out[o:o + n].view(torch.bfloat16).view(rows, Hl, cfg.D) for o, n in outs[:cfg.cp]]
-        lse_outs = [dev_out[o:o + n].view(torch.float32).view(rows, Hl) for o, n in outs[cfg.cp:]]
-        calls.append((rows, srcs, lses, dsts, lse_outs))
+    host_out = [torch.empty(off_out, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    # Two device arenas per direction, so that step k+1's inputs can arrive
+    # and step k-1's results can leave while step k merges.
+    dev_in = [torch.empty(off_in, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    dev_out = [torch.empty(off_out, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    calls = [[], []]
+    for k in range(2):
+        for rows, ins, outs in plan:
+            srcs = [dev_in[k][o:o + n].view(torch.bfloat16).view(rows, cfg.H, cfg.D) for o, n in ins[:cfg.cp]]
+            lses = [dev_in[k][o:o + n].view(torch.float32).view(rows, cfg.H) for o, n in ins[cfg.cp:]]
+            dsts = [dev_out[k][o:o + n].view(torch.bfloat16).view(rows, Hl, cfg.D) for o, n in outs[:cfg.cp]]
+            lse_outs = [dev_out[k][o:o + n].view(torch.float32).view(rows, Hl) for o, n in outs[cfg.cp:]]
+            calls[k].append((rows, srcs, lses, dsts, lse_outs))
+    s_h2d, s_cmp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    done_merge = [torch.cuda.Event(), torch.cuda.Event()]   # the merges of the step in slot k are done
+    done_d2h = [torch.cuda.Event(), torch.cuda.Event()]     # slot k's results have left
+    landed = [torch.cuda.Event(), torch.cuda.Event()]       # slot k's inputs have arrived
 
-    def step():
-        dev_in.copy_(host_in, non_blocking=True)
-        for rows, srcs, lses, dsts, lse_outs in calls:
-            dcp.dcp_lse_reduce(srcs, lses, cfg.H, cfg.cp, rows, cfg.H, cfg.D, cfg.lse_base_e, dsts, lse_outs)
-        host_out.copy_(dev_out, non_blocking=True)
+    def run(steps):
+        for k in range(steps):
+            b = k & 1
+            with torch.cuda.stream(s_h2d):
+                if k >= 2:
+                    s_h2d.wait_event(done_merge[b])  # slot b's inputs were read by step k-2
+                dev_in[b].copy_(host_in, non_blocking=True)
+                landed[b].record(s_h2d)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(landed[b])
+                if k >= 2:
+                    s_cmp.wait_event(done_d2h[b])  # slot b's outputs of step k-2 have left
+                for rows, srcs, lses, dsts, lse_outs in calls[b]:
+                    dcp.dcp_lse_reduce(srcs, lses, cfg.H, cfg.cp, rows, cfg.H, cfg.D, cfg.lse_base_e, dsts,
+                                       lse_outs, stream=s_cmp)
+                done_merge[b].record(s_cmp)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(done_merge[b])
+                host_out[b].copy_(dev_out[b], non_blocking=True)
+                done_d2h[b].record(s_d2h)
 
-    for _ in range(3):
-        step()
+    run(3)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        step()
-    b.record()
+    main = torch.cuda.current_stream()
+    a.record(main)
+    for st in (s_h2d, s_cmp, s_d2h):
+        st.wait_stream(main)
+    run(steps)
+    for st in (s_h2d, s_cmp, s_d2h):
+        main.wait_stream(st)
+    b.record(main)
     b.synchronize()
     sec = a.elapsed_time(b) * 1e-3
     tot_sec, tot_bytes = aggregate_ranks(sec, float(nbytes * steps))
     return {"value": round(tot_bytes / tot_sec / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": off_in,
             "d2h_bytes_per_step": off_out, "ms_per_step": round(tot_sec * 1e3 / steps, 4),
-            "how": "one pinned host -> device copy of the step's inputs, dcp_lse_reduce for each row count, "
-                   "one device -> pinned host copy of the step's outputs; eager, timed with CUDA events"}
+            "how": "per step: one pinned host -> device copy of the step's inputs, dcp_lse_reduce for each row "
+                   "count, one device -> pinned host copy of the step's outputs; copies and merges on three "
+                   "streams with two arenas each, so consecutive steps overlap; timed with CUDA events"}
 
 
 def cpu_baseline(cfg, budget_s: float = 12.0):
