@@ -494,15 +494,16 @@ struct WarpReduceScatter {
     }
 };
 
-// Per-head reduction over the CTA's 128 token-threads of v[kNH]; results land in
-// out[kNH] in shared memory (red is a [4][kNH] scratch area).
-template <int kNH, bool kSum>
-__device__ __forceinline__ void cta_reduce_heads(float* v, int warp, int lane, float* red, float* out) {
-    constexpr int kFinal = kNH / 32 > 1 ? kNH / 32 : 1;
-    WarpReduceScatter<kNH, 16, kSum>::run(v, lane);
-    const int h0 = (lane / (32 * kFinal / kNH)) * kFinal;
+// Per-head reduction over the tile's 128 tokens. Each thread holds v[kHW] for
+// heads [hb, hb + kHW) of its token (TMEM lane quadrant `quad`); the kNH
+// results land in out[kNH] in shared memory (red is a [4][kNH] scratch area).
+template <int kNH, int kHW, bool kSum>
+__device__ __forceinline__ void cta_reduce_heads(float* v, int quad, int hb, int lane, float* red, float* out) {
+    constexpr int kFinal = kHW / 32 > 1 ? kHW / 32 : 1;
+    WarpReduceScatter<kHW, 16, kSum>::run(v, lane);
+    const int h0 = (lane / (32 * kFinal / kHW)) * kFinal;
 #pragma unroll
-    for (int e = 0; e < kFinal; ++e) red[warp * kNH + h0 + e] = v[e];
+    for (int e = 0; e < kFinal; ++e) red[quad * kNH + hb + h0 + e] = v[e];
     __syncthreads();
     if (threadIdx.x < kNH) {
         const int h = threadIdx.x;
@@ -512,8 +513,14 @@ __device__ __forceinline__ void cta_reduce_heads(float* v, int warp, int lane, f
     __syncthreads();
 }
 
+// Threads of the tcgen05 kernel: one per (token, group of heads); with 32 or
+// more heads per CTA each token's heads are split over two threads.
+template <int kNH>
+__host__ __device__ constexpr int tc_head_groups() { return kNH >= 32 ? 2 : 1; }
+
 template <int kDk, int kNH>
-__global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc_kernel(const __grid_constant__ TcParams p) {
+    constexpr int kHW = kNH / tc_head_groups<kNH>();  // heads per thread
     constexpr int kAtoms = kDk / 64;            // 64-wide slices of a row: 9 (Dk 576) or 8 (Dk 512)
     constexpr int kQAtom = kNH * 128;           // bytes of one Q slice
     constexpr bool kPInRope = kAtoms == 9;      // P^T reuses the RoPE slice's buffer
@@ -565,7 +572,10 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tlane = (uint32_t)(32 * warp) << 16;
+    // warp w reads TMEM lane quadrant w % 4 (tokens 32(w%4) .. +31) and
+    // handles heads [hb, hb + kHW) of those tokens
+    const int quad = warp & 3, tok = tid & 127, hb = (warp >> 2) * kHW;
+    const uint32_t tlane = (uint32_t)(32 * quad) << 16;
 
     pdl_wait();
     pdl_launch_dependents();
@@ -581,7 +591,7 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
     const int64_t out_row0 = ((int64_t)b * p.H + h0) * kDv;
 
     if (ntok == 0) {  // empty range: output 0, LSE -inf
-        for (int i = tid; i < kNH * kDv / 8; i += 128)
+        for (int i = tid; i < kNH * kDv / 8; i += (int)blockDim.x)
             reinterpret_cast<uint4*>(out + out_row0 * 2)[i] = make_uint4(0u, 0u, 0u, 0u);
         if (tid < kNH) lse[(int64_t)b * p.H + h0 + tid] = -INFINITY;
     } else {
@@ -593,9 +603,9 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
             mbar_expect_tx(bar_kv, (uint32_t)(kAtoms * kTcAtom));
             for (int a = 0; a < kAtoms; ++a) tma_load_2d(kv_s + a * kTcAtom, &p.tm_kv[shard], a * 64, row0, bar_kv);
         }
-        float l_part[kNH];  // this token-thread's share of each head's sum
+        float l_part[kHW];  // this thread's token's share of each of its heads' sums
 #pragma unroll
-        for (int h = 0; h < kNH; ++h) l_part[h] = 0.f;
+        for (int h = 0; h < kHW; ++h) l_part[h] = 0.f;
         mbar_wait(bar_q, 0, p.status);
 
         for (int i = 0; i < ntiles; ++i) {
@@ -617,28 +627,29 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
             mbar_wait(bar_s, ph, p.status);
             tc_fence_after();
 
-            float sv[kNH];
+            float sv[kHW];
 #pragma unroll
-            for (int c = 0; c < kNH; c += 16) tmem_ld16(tmem + tlane + c, sv + c);
+            for (int c = 0; c < kHW; c += 16) tmem_ld16(tmem + tlane + hb + c, sv + c);
             tmem_wait_ld();
             const int valid = (ntok - i * kTcTok) < kTcTok ? (ntok - i * kTcTok) : kTcTok;
-            const bool live = tid < valid;
+            const bool live = tok < valid;
 #pragma unroll
-            for (int h = 0; h < kNH; ++h) sv[h] = live ? sv[h] * p.scale_log2 : -INFINITY;
+            for (int h = 0; h < kHW; ++h) sv[h] = live ? sv[h] * p.scale_log2 : -INFINITY;
             if (!live) {  // a token past the range: its value row must be finite (0 x V)
+                constexpr int kPerGroup = 8 / tc_head_groups<kNH>();  // latent slices zeroed per thread
 #pragma unroll 1
-                for (int a = 0; a < 8; ++a) {
-                    uint4* row = reinterpret_cast<uint4*>(kv_s + a * kTcAtom + (tid >> 3) * 1024 + (tid & 7) * 128);
+                for (int a = (warp >> 2) * kPerGroup; a < (warp >> 2) * kPerGroup + kPerGroup; ++a) {
+                    uint4* row = reinterpret_cast<uint4*>(kv_s + a * kTcAtom + (tok >> 3) * 1024 + (tok & 7) * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             // per-head maximum over the tile's tokens
             {
-                float mx[kNH];
+                float mx[kHW];
 #pragma unroll
-                for (int h = 0; h < kNH; ++h) mx[h] = sv[h];
-                cta_reduce_heads<kNH, false>(mx, warp, lane, red, t_s);
+                for (int h = 0; h < kHW; ++h) mx[h] = sv[h];
+                cta_reduce_heads<kNH, kHW, false>(mx, quad, hb, lane, red, t_s);
             }
             // move the running max only when some head's tile max exceeds it by more than 2^8
             const bool need = tid < kNH && t_s[tid] > m_s[tid] + 8.f;
@@ -659,7 +670,7 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
 #pragma unroll 1
                 for (int m = 0; m < 4; ++m) {
 #pragma unroll
-                    for (int c = 0; c < kNH; c += 16) {
+                    for (int c = hb; c < hb + kHW; c += 16) {
                         float ov[16];
                         tmem_ld16(tmem + tlane + kNH + m * kNH + c, ov);
                         tmem_wait_ld();
@@ -674,8 +685,8 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
             // (the shared reads all come before the stores, so none waits behind one)
             {
 #pragma unroll
-                for (int h = 0; h < kNH; h += 4) {
-                    const float4 mv = *reinterpret_cast<const float4*>(m_s + h);
+                for (int h = 0; h < kHW; h += 4) {
+                    const float4 mv = *reinterpret_cast<const float4*>(m_s + hb + h);
                     sv[h] = ex2(sv[h] - mv.x);
                     sv[h + 1] = ex2(sv[h + 1] - mv.y);
                     sv[h + 2] = ex2(sv[h + 2] - mv.z);
@@ -683,8 +694,8 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
                 }
                 if (any) {
 #pragma unroll
-                    for (int h = 0; h < kNH; h += 4) {
-                        const float4 av = *reinterpret_cast<const float4*>(a_s + h);
+                    for (int h = 0; h < kHW; h += 4) {
+                        const float4 av = *reinterpret_cast<const float4*>(a_s + hb + h);
                         l_part[h] = l_part[h] * av.x + sv[h];
                         l_part[h + 1] = l_part[h + 1] * av.y + sv[h + 1];
                         l_part[h + 2] = l_part[h + 2] * av.z + sv[h + 2];
@@ -692,13 +703,13 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
                     }
                 } else {
 #pragma unroll
-                    for (int h = 0; h < kNH; ++h) l_part[h] += sv[h];
+                    for (int h = 0; h < kHW; ++h) l_part[h] += sv[h];
                 }
-                uint8_t* const prow = p_s + (tid >> 6) * kQAtom;
-                const int tl = tid & 63;
+                uint8_t* const prow = p_s + (tok >> 6) * kQAtom;
+                const int tl = tok & 63;
 #pragma unroll
-                for (int h = 0; h < kNH; ++h)
-                    *reinterpret_cast<__nv_bfloat16*>(prow + sw128(h, tl)) = __float2bfloat16_rn(sv[h]);
+                for (int h = 0; h < kHW; ++h)
+                    *reinterpret_cast<__nv_bfloat16*>(prow + sw128(hb + h, tl)) = __float2bfloat16_rn(sv[h]);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
@@ -727,7 +738,7 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
         // final sums, then normalise, round to bf16 and store; LSE = m + log2(l)
         mbar_wait(bar_o, (uint32_t)((ntiles - 1) & 1), p.status);
         tc_fence_after();
-        cta_reduce_heads<kNH, true>(l_part, warp, lane, red, t_s);
+        cta_reduce_heads<kNH, kHW, true>(l_part, quad, hb, lane, red, t_s);
         // The [kNH, 512] output tile is assembled in the KV buffer (free now:
         // every MMA is done and no load is pending), then leaves in one bulk
         // copy: rows h0 .. h0+kNH-1 of out[b] are contiguous.
@@ -735,11 +746,11 @@ __global__ void __launch_bounds__(128, 1) mla_partial_tc_kernel(const __grid_con
 #pragma unroll 1
         for (int m = 0; m < 4; ++m) {
 #pragma unroll
-            for (int c = 0; c < kNH; c += 16) {
+            for (int c = hb; c < hb + kHW; c += 16) {
                 float ov[16];
                 tmem_ld16(tmem + tlane + kNH + m * kNH + c, ov);
                 tmem_wait_ld();
-                const int dv = 128 * m + 32 * warp + lane;
+                const int dv = 128 * m + 32 * quad + lane;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) o_s[(c + j) * kDv + dv] = __float2bfloat16_rn(ov[j] / t_s[c + j]);
             }
@@ -842,7 +853,7 @@ cudaError_t launch_tc(const TcParams& prm, int64_t B, int n_slots, unsigned flag
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)n_slots, (unsigned)(prm.H / kNH), (unsigned)B);
-    cfg.blockDim = dim3(128, 1, 1);
+    cfg.blockDim = dim3(128 * tc_head_groups<kNH>(), 1, 1);
     cfg.dynamicSmemBytes = bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
