@@ -40,9 +40,13 @@ constexpr int kSPad = 4;             // fp32 padding of a score row in shared me
 constexpr unsigned kFlagPdl = 1u;
 constexpr unsigned kFlagMmaSync = 2u;   // DCP_MLA_FLAG_MMA_SYNC
 constexpr unsigned kFlagTcgen05 = 4u;   // DCP_MLA_FLAG_TCGEN05
-// Below this many tokens per (row, split) the tcgen05 kernel's per-CTA set-up
-// (TMEM, a 72 KB Q load, one 224 KB CTA per SM) outweighs its faster tiles.
-constexpr int64_t kTcMinTokensPerSplit = 256;
+// When the tcgen05 kernel is the default. Its MMAs cost about the same per
+// instruction whatever the head block (N = 16, 32 or 64), so it pays off with
+// 64-head blocks from one full 128-token tile per (row, split), with 32-head
+// blocks from two, and never with 16-head blocks, where the mma.sync kernel is
+// faster at every measured length.
+constexpr int64_t kTcMinTokensH64 = 128;
+constexpr int64_t kTcMinTokensH32 = 256;
 constexpr long long kWaitLimitNs = 2000000000LL;
 
 constexpr int kSlots = 16;            // (shard, split) outputs of one launch
@@ -882,6 +886,12 @@ extern "C" int dcp_mla_decode_smem_bytes(int Dk, int H) {
 
 namespace {
 
+bool tc_is_default(int H, int64_t tokens_per_split) {
+    if (H % 64 == 0) return tokens_per_split >= kTcMinTokensH64;
+    if (H % 32 == 0) return tokens_per_split >= kTcMinTokensH32;
+    return false;
+}
+
 // Validate and launch the producer over n_shard shards x n_split splits
 // (slot = shard * n_split + split), all in one grid.
 int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv_len_ptrs, int n_shard, int64_t B,
@@ -919,7 +929,7 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
     if (B == 0) return 0;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool use_tc = (flags & kFlagTcgen05) != 0 ||
-                        (!(flags & kFlagMmaSync) && (T + n_split - 1) / n_split >= kTcMinTokensPerSplit);
+                        (!(flags & kFlagMmaSync) && tc_is_default(H, (T + n_split - 1) / n_split));
     if (use_tc) {  // the tcgen05 kernel
         TcParams tp;
         const int nh = H % 64 == 0 ? 64 : (H % 32 == 0 ? 32 : 16);

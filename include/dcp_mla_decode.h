@@ -82,9 +82,10 @@ enum {
 /*
  * Flags of the producer and the fused decode (besides DCP_FLAG_PDL = 1). By
  * default the producer runs the tcgen05 kernel (TMEM accumulators, TMA loads)
- * when a split holds at least 256 tokens of the cache (ceil(T / n_split) >=
- * 256) and the warp-level mma.sync kernel otherwise; these flags force one.
- * Both compute the same partials within the stated tolerances.
+ * when H is a multiple of 64 and a split holds at least 128 tokens of the
+ * cache (ceil(T / n_split) >= 128), or H is a multiple of 32 and a split
+ * holds at least 256; otherwise the warp-level mma.sync kernel. These flags
+ * force one. Both compute the same partials within the stated tolerances.
  */
 #define DCP_MLA_FLAG_MMA_SYNC 2u
 #define DCP_MLA_FLAG_TCGEN05 4u
