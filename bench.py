@@ -441,7 +441,9 @@ def mla_extras(hbm_peak, tensor_peak):
             "gbs": round(nbytes / us / 1e3, 1), "tflops": round(flops / us / 1e6, 1),
             "frac_of_measured_hbm": round(nbytes / us / 1e3 / hbm_peak, 4),
             "frac_of_measured_bf16_tensor": round(flops / us / 1e6 / tensor_peak, 4),
-            "kernel": "tcgen05", "mma_sync_kernel_us_per_call": round(us_mma, 2)}
+            "kernel": {dcp.DCP_MLA_KERNEL_TCGEN05: "tcgen05", dcp.DCP_MLA_KERNEL_MMA_SYNC: "mma.sync"}[
+                dcp.dcp_mla_decode_kernel(H, T, ns, dcp.DCP_FLAG_PDL)],
+            "mma_sync_kernel_us_per_call": round(us_mma, 2)}
         # fused: the same cache split over cp shards of T/cp tokens each
         Ts = T // cp
         shard_kvs = [[kvs[k][:, j * Ts:(j + 1) * Ts].contiguous() for j in range(cp)] for k in range(n_calls)]

@@ -16,6 +16,7 @@ from __future__ import annotations
 
 from ._binding import (DCP_DTYPE_BF16, DCP_DTYPE_F16, DCP_FLAG_LSE_FIRST, DCP_FLAG_PDL, DCP_FLAG_PRELOAD,
                        DCP_LSE_REDUCE_CP_MAX, DCP_MLA_FLAG_MMA_SYNC, DCP_MLA_FLAG_TCGEN05, DCP_MLA_SPLIT_MAX,
+                       DCP_MLA_KERNEL_MMA_SYNC, DCP_MLA_KERNEL_TCGEN05, dcp_mla_decode_kernel,
                        EXPORTED_SYMBOLS, DcpError,
                        Layout,
                        dcp_lse_reduce, dcp_lse_reduce_ex, dcp_lse_reduce_strerror, dcp_lse_reduce_version,
@@ -29,7 +30,7 @@ __all__ = ["dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dc
            "DCP_MLA_NOALLOC_SCRATCH_BYTES", "DCP_MLA_FLAG_MMA_SYNC", "DCP_MLA_FLAG_TCGEN05",
            "algorithmic_bytes", "Layout", "DcpError", "load", "library_path", "EXPORTED_SYMBOLS",
            "DCP_DTYPE_BF16", "DCP_DTYPE_F16", "DCP_FLAG_PDL", "DCP_FLAG_PRELOAD", "DCP_FLAG_LSE_FIRST",
-           "DCP_LSE_REDUCE_CP_MAX"]
+           "DCP_LSE_REDUCE_CP_MAX", "dcp_mla_decode_kernel", "DCP_MLA_KERNEL_TCGEN05", "DCP_MLA_KERNEL_MMA_SYNC"]
 
 
 def algorithmic_bytes(cp: int, B: int, H: int, D: int, elem: int = 2, skipped_payload_rows: int = 0) -> int:

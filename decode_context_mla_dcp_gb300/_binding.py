@@ -24,11 +24,13 @@ DCP_FLAG_LSE_FIRST = 4
 
 EXPORTED_SYMBOLS = ("dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dcp_lse_reduce_version",
                     "dcp_mla_decode_partial", "dcp_mla_decode_smem_bytes", "dcp_mla_decode_workspace_bytes",
-                    "dcp_mla_decode", "dcp_mla_decode_noalloc")
+                    "dcp_mla_decode", "dcp_mla_decode_noalloc", "dcp_mla_decode_kernel")
 DCP_MLA_NOALLOC_SCRATCH_BYTES = 32 << 20
 DCP_MLA_SPLIT_MAX = 16
 DCP_MLA_FLAG_MMA_SYNC = 2
 DCP_MLA_FLAG_TCGEN05 = 4
+DCP_MLA_KERNEL_TCGEN05 = 1
+DCP_MLA_KERNEL_MMA_SYNC = 2
 _MLA_ERRORS = {-101: "q, kv, kv_len, out_ptrs, lse_ptrs or an entry is NULL",
                -102: "B must be in [0, 65535], T >= 0, H a positive multiple of 16, Dk 512 or 576, Dv 512",
                -103: "n_split must be in [1, 16]",
@@ -93,6 +95,8 @@ def load(path: str | None = None):
         lib.dcp_mla_decode_partial.restype = ci
         lib.dcp_mla_decode_smem_bytes.argtypes = [ci, ci]
         lib.dcp_mla_decode_smem_bytes.restype = ci
+        lib.dcp_mla_decode_kernel.argtypes = [ci, i64, ci, ctypes.c_uint]
+        lib.dcp_mla_decode_kernel.restype = ci
         lib.dcp_mla_decode_workspace_bytes.argtypes = [ci, ci, i64, ci, ci]
         lib.dcp_mla_decode_workspace_bytes.restype = i64
         lib.dcp_mla_decode.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ci, i64, ci, ci, ci, i64,
@@ -185,6 +189,15 @@ def dcp_mla_decode_partial(q, kv, kv_len, B: int, H: int, Dk: int, Dv: int, T: i
 
 def dcp_mla_decode_smem_bytes(Dk: int, H: int) -> int:
     return int(load().dcp_mla_decode_smem_bytes(int(Dk), int(H)))
+
+
+def dcp_mla_decode_kernel(H: int, T: int, n_split: int, flags: int = 0) -> int:
+    """DCP_MLA_KERNEL_TCGEN05 or DCP_MLA_KERNEL_MMA_SYNC: the producer kernel
+    these arguments select (host only; raises DcpError for invalid ones)."""
+    k = int(load().dcp_mla_decode_kernel(int(H), int(T), int(n_split), int(flags)))
+    if k < 0:
+        _check(k)
+    return k
 
 
 def dcp_mla_decode_workspace_bytes(cp: int, n_split: int, B: int, H: int, Dv: int = 512) -> int:

@@ -878,10 +878,13 @@ cudaError_t launch_tc_dk(const TcParams& prm, int64_t B, int n_slots, unsigned f
 }  // namespace
 
 extern "C" int dcp_mla_decode_smem_bytes(int Dk, int H) {
+    if ((Dk != 512 && Dk != 576) || H < 16 || H % 16 != 0) return -1;
     const int g = H % 64 == 0 ? 4 : (H % 32 == 0 ? 2 : 1);
-    if (Dk == 576) return g == 4 ? smem_bytes<576, 4>() : (g == 2 ? smem_bytes<576, 2>() : smem_bytes<576, 1>());
-    if (Dk == 512) return g == 4 ? smem_bytes<512, 4>() : (g == 2 ? smem_bytes<512, 2>() : smem_bytes<512, 1>());
-    return -1;
+    const int mma = Dk == 576 ? (g == 4 ? smem_bytes<576, 4>() : (g == 2 ? smem_bytes<576, 2>() : smem_bytes<576, 1>()))
+                              : (g == 4 ? smem_bytes<512, 4>() : (g == 2 ? smem_bytes<512, 2>() : smem_bytes<512, 1>()));
+    const int tc = Dk == 576 ? (g == 4 ? tc_smem_bytes<576, 64>() : (g == 2 ? tc_smem_bytes<576, 32>() : tc_smem_bytes<576, 16>()))
+                             : (g == 4 ? tc_smem_bytes<512, 64>() : (g == 2 ? tc_smem_bytes<512, 32>() : tc_smem_bytes<512, 16>()));
+    return mma > tc ? mma : tc;
 }
 
 namespace {
@@ -891,6 +894,20 @@ bool tc_is_default(int H, int64_t tokens_per_split) {
     if (H % 32 == 0) return tokens_per_split >= kTcMinTokensH32;
     return false;
 }
+
+}  // namespace
+
+extern "C" int dcp_mla_decode_kernel(int H, int64_t T, int n_split, unsigned flags) {
+    if (H < 16 || H % 16 != 0 || T < 0) return DCP_MLA_ERR_BAD_SHAPE;
+    if (n_split < 1 || n_split > DCP_MLA_SPLIT_MAX) return DCP_MLA_ERR_BAD_SPLIT;
+    if ((flags & ~(kFlagPdl | kFlagMmaSync | kFlagTcgen05)) != 0) return DCP_MLA_ERR_BAD_FLAGS;
+    if ((flags & kFlagMmaSync) && (flags & kFlagTcgen05)) return DCP_MLA_ERR_BAD_FLAGS;
+    if (flags & kFlagTcgen05) return DCP_MLA_KERNEL_TCGEN05;
+    if (flags & kFlagMmaSync) return DCP_MLA_KERNEL_MMA_SYNC;
+    return tc_is_default(H, (T + n_split - 1) / n_split) ? DCP_MLA_KERNEL_TCGEN05 : DCP_MLA_KERNEL_MMA_SYNC;
+}
+
+namespace {
 
 // Validate and launch the producer over n_shard shards x n_split splits
 // (slot = shard * n_split + split), all in one grid.
@@ -928,8 +945,7 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
     }
     if (B == 0) return 0;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool use_tc = (flags & kFlagTcgen05) != 0 ||
-                        (!(flags & kFlagMmaSync) && tc_is_default(H, (T + n_split - 1) / n_split));
+    const bool use_tc = dcp_mla_decode_kernel(H, T, n_split, flags) == DCP_MLA_KERNEL_TCGEN05;
     if (use_tc) {  // the tcgen05 kernel
         TcParams tp;
         const int nh = H % 64 == 0 ? 64 : (H % 32 == 0 ? 32 : 16);

@@ -95,8 +95,24 @@ int dcp_mla_decode_partial(const void* q, const void* kv, const int32_t* kv_len,
                            int n_split, void* const* out_ptrs, float* const* lse_ptrs,
                            int32_t* status, unsigned flags, void* stream);
 
-/* Dynamic shared memory one CTA of the kernel uses for Dk (bytes), for sizing. */
+/*
+ * Dynamic shared memory one CTA of the producer may use for Dk and H (bytes):
+ * the larger of the two kernels' needs. -1 for Dk not 512 or 576, or H not a
+ * positive multiple of 16.
+ */
 int dcp_mla_decode_smem_bytes(int Dk, int H);
+
+/*
+ * Which kernel dcp_mla_decode_partial (and dcp_mla_decode, per shard) runs
+ * for H heads, T cache tokens per row, n_split splits and these flags:
+ * DCP_MLA_KERNEL_TCGEN05 or DCP_MLA_KERNEL_MMA_SYNC. Host only; launches
+ * nothing. Returns DCP_MLA_ERR_BAD_SHAPE (H not a positive multiple of 16,
+ * T < 0), DCP_MLA_ERR_BAD_SPLIT or DCP_MLA_ERR_BAD_FLAGS for arguments the
+ * producer would reject for those reasons.
+ */
+#define DCP_MLA_KERNEL_TCGEN05 1
+#define DCP_MLA_KERNEL_MMA_SYNC 2
+int dcp_mla_decode_kernel(int H, int64_t T, int n_split, unsigned flags);
 
 /*
  * Bytes of caller-provided workspace dcp_mla_decode needs: the cp*n_split

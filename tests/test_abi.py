@@ -152,3 +152,29 @@ def test_fused_decode_rejects_bad_workspace_and_cp(lib):
     assert call(n_split=8) == -107          # 4 * 8 sources > 16
     assert call(H=36) == -107               # 36 % 8 != 0
     assert call(cp=0) == -107
+
+
+def test_producer_kernel_choice(lib):
+    """The producer's default kernel by head block and split length, the
+    forcing flags, and rejected arguments (host only)."""
+    tc, mma = dcp.DCP_MLA_KERNEL_TCGEN05, dcp.DCP_MLA_KERNEL_MMA_SYNC
+    k = dcp.dcp_mla_decode_kernel
+    # 64-head blocks: tcgen05 from one full 128-token tile per split
+    assert k(128, 4096, 9) == tc and k(64, 4096, 16) == tc and k(64, 2048, 16) == tc
+    assert k(64, 2032, 16) == mma and k(128, 100, 1) == mma  # ceil(2032 / 16) = 127 tokens per split
+    # 32-head blocks: from two tiles
+    assert k(32, 2048, 8) == tc and k(96, 2048, 8) == tc and k(32, 2040, 8) == mma and k(32, 1024, 8) == mma
+    # 16-head blocks: always mma.sync by default
+    assert k(16, 1 << 20, 1) == mma and k(48, 1 << 20, 1) == mma
+    # forcing flags (PDL does not change the choice)
+    assert k(16, 64, 1, dcp.DCP_MLA_FLAG_TCGEN05) == tc and k(128, 1 << 20, 1, dcp.DCP_MLA_FLAG_MMA_SYNC) == mma
+    assert k(128, 4096, 1, dcp.DCP_FLAG_PDL) == tc
+    for args, status in [((128, 4096, 1, dcp.DCP_MLA_FLAG_TCGEN05 | dcp.DCP_MLA_FLAG_MMA_SYNC), -105),
+                         ((128, 4096, 1, 8), -105), ((128, 4096, 0), -103), ((128, 4096, 17), -103),
+                         ((20, 4096, 1), -102), ((128, -1, 1), -102)]:
+        with pytest.raises(dcp.DcpError) as e:
+            k(*args)
+        assert e.value.status == status
+    # the shared-memory query covers the larger (tcgen05) kernel
+    assert dcp.dcp_mla_decode_smem_bytes(576, 64) == 224256  # 144 KB tile + 72 KB Q + misc + alignment
+    assert dcp.dcp_mla_decode_smem_bytes(500, 64) == -1 and dcp.dcp_mla_decode_smem_bytes(576, 20) == -1
