@@ -331,3 +331,25 @@ def test_running_max_jumps_rescale_the_output(oracle_mod, H, Dk, kflags):
         ref_o, ref_l = oracle_partials(q, kv, lens, 1, MLA_SCALE, base_e)
         check_out(outs[0], ref_o[0], f"H={H} base_e={base_e}")
         check_lse(lses[0], ref_l[0], f"H={H} base_e={base_e}")
+
+
+@pytest.mark.parametrize("H,T,n_split", [(64, 1024, 4), (64, 500, 4), (32, 1024, 4), (32, 1024, 8), (16, 2048, 1),
+                                         (128, 256, 2)])
+def test_default_call_runs_the_kernel_the_query_names(H, T, n_split):
+    """dcp_mla_decode_kernel names the kernel a default call launches: the
+    default call's outputs equal, bit for bit, those of the call forcing it."""
+    B = 3
+    q, kv = make_mla_inputs(B, H, T, 576, seed=H + T + n_split)
+    lens = torch.tensor([T, T - 7, 1], dtype=torch.int32, device="cuda")
+    which = dcp.dcp_mla_decode_kernel(H, T, n_split)
+    force = dcp.DCP_MLA_FLAG_TCGEN05 if which == dcp.DCP_MLA_KERNEL_TCGEN05 else dcp.DCP_MLA_FLAG_MMA_SYNC
+    a_o, a_l = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), lens, MLA_SCALE, n_split=n_split)
+    b_o, b_l = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), lens, MLA_SCALE, n_split=n_split, flags=force)
+    torch.cuda.synchronize()
+    for s in range(n_split):
+        assert torch.equal(a_o[s], b_o[s]) and torch.equal(a_l[s], b_l[s]), f"split {s}"
+    # and the other kernel rounds differently somewhere, so the identity above is not vacuous
+    other = dcp.DCP_MLA_FLAG_MMA_SYNC if force == dcp.DCP_MLA_FLAG_TCGEN05 else dcp.DCP_MLA_FLAG_TCGEN05
+    c_o, _ = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), lens, MLA_SCALE, n_split=n_split, flags=other)
+    torch.cuda.synchronize()
+    assert any(not torch.equal(a_o[s], c_o[s]) for s in range(n_split))
