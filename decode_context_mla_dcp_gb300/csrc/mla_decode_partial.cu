@@ -439,6 +439,13 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Bring a box of the tensor into L2 ahead of its load (a hint: no shared
+// memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
@@ -615,6 +622,12 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
         for (int i = 0; i < ntiles; ++i) {
             const uint32_t ph = (uint32_t)(i & 1);
             mbar_wait(bar_kv, ph, p.status);
+            // Start the next tile's DRAM reads now, into L2 (from a thread of another
+            // warp than the MMA issuer's), so that its load after this tile's value
+            // MMAs streams from L2: every CTA reloads at about the same moment, and
+            // from DRAM those loads contend.
+            if (tid == 32 && i + 1 < ntiles)
+                for (int a = 0; a < kAtoms; ++a) tma_prefetch_2d(&p.tm_kv[shard], a * 64, row0 + (i + 1) * kTcTok);
             if (tid == 0) {  // scores: S^T = K_tile . Q^T
                 tc_fence_after();
 #pragma unroll 1
