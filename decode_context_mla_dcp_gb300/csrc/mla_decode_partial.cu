@@ -389,12 +389,15 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
 // Q and each KV tile arrive by TMA in 128-byte-swizzled 64-wide slices; the KV
 // slices serve as the K-major A operand of the scores and, read along the
 // latent dims, as the M-major A operand of the values. TMEM holds S^T (kNH
-// columns) and O^T (4 x kNH columns). Thread t of the 128 owns token t: it reads
-// its score row, the per-head maxima over the tile come from a reduce-scatter
-// butterfly across lanes and shared memory, and the running maximum moves only
-// when a head's tile maximum exceeds it by more than 2^8 (then O^T is rescaled
-// in TMEM), so the rescale is rare. P^T (bf16) is written into the RoPE slice's
-// buffer once the scores are done (into its own buffer when Dk = 512).
+// columns) and O^T (4 x kNH columns). A thread owns one token of the tile and
+// its heads (all kNH of them, or half when kNH >= 32: then warp w reads TMEM
+// lane quadrant w % 4 for head half w / 4). The per-head maxima over the tile
+// come from a reduce-scatter butterfly across lanes and shared memory, and the
+// running maximum moves only when a head's tile maximum exceeds it by more
+// than 2^8 (then O^T is rescaled in TMEM), so the rescale is rare. P^T (bf16)
+// is written into the RoPE slice's buffer once the scores are done (into its
+// own buffer when Dk = 512). The next tile is prefetched into L2 as soon as
+// a tile lands, so its reload streams from L2.
 
 constexpr int kTcTok = 128;                  // tokens per tile
 constexpr int kTcAtom = kTcTok * 128;        // one 64-wide slice of 128 token rows (bytes)
