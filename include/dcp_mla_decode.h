@@ -139,8 +139,10 @@ int64_t dcp_mla_decode_workspace_bytes(int cp, int n_split, int64_t B, int H, in
  * shards' tokens): "[DCP] Optimize shared Output, Query, and Indexer/Top-K via
  * peer memory" (sglang #32851), commit notes on the interleaved KV shards and
  * the cross-rank combine; on one GPU the shards are local buffers and the
- * exchange is the merge's strided read. cp launches of the producer and one
- * merge are enqueued on `stream` (PDL between them with DCP_FLAG_PDL).
+ * exchange is the merge's strided read. One launch of the producer (covering
+ * every shard and split) and one merge are enqueued on `stream` (PDL between
+ * them with DCP_FLAG_PDL); the producer kernel per dcp_mla_decode_kernel(H,
+ * T, n_split, flags).
  * Constraints: cp*n_split <= 16 and H a multiple of cp*n_split and of 16.
  */
 int dcp_mla_decode(const void* q, const void* const* kv_ptrs, const int32_t* const* kv_len_ptrs, int cp,
