@@ -404,7 +404,7 @@ def mla_extras(hbm_peak, tensor_peak):
     out = {}
     n_calls, B, T = 10, 8, 4096
     # split counts chosen so that one launch is about one wave of one-CTA-per-SM blocks
-    for name, H, cp, n_split, ns in (("deepseek-v2 shard, 128 heads", 128, 8, 2, 9),
+    for name, H, cp, n_split, ns in (("deepseek-v2 shard, 128 heads", 128, 8, 1, 9),
                                      ("kimi-k2.5 shard, 64 heads", 64, 4, 4, 16)):
         q = torch.randn((B, H, 576), generator=gen, device="cuda").to(torch.bfloat16)
         kvs = [torch.randn((B, T, 576), generator=gen, device="cuda").to(torch.bfloat16) for _ in range(n_calls)]
