@@ -17,6 +17,7 @@ from __future__ import annotations
 from ._binding import (DCP_DTYPE_BF16, DCP_DTYPE_F16, DCP_FLAG_LSE_FIRST, DCP_FLAG_PDL, DCP_FLAG_PRELOAD,
                        DCP_LSE_REDUCE_CP_MAX, DCP_MLA_FLAG_MMA_SYNC, DCP_MLA_FLAG_TCGEN05, DCP_MLA_SPLIT_MAX,
                        DCP_MLA_KERNEL_MMA_SYNC, DCP_MLA_KERNEL_TCGEN05, dcp_mla_decode_kernel,
+                       dcp_mla_decode_pick_split,
                        EXPORTED_SYMBOLS, DcpError,
                        Layout,
                        dcp_lse_reduce, dcp_lse_reduce_ex, dcp_lse_reduce_strerror, dcp_lse_reduce_version,
@@ -30,7 +31,8 @@ __all__ = ["dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dc
            "DCP_MLA_NOALLOC_SCRATCH_BYTES", "DCP_MLA_FLAG_MMA_SYNC", "DCP_MLA_FLAG_TCGEN05",
            "algorithmic_bytes", "Layout", "DcpError", "load", "library_path", "EXPORTED_SYMBOLS",
            "DCP_DTYPE_BF16", "DCP_DTYPE_F16", "DCP_FLAG_PDL", "DCP_FLAG_PRELOAD", "DCP_FLAG_LSE_FIRST",
-           "DCP_LSE_REDUCE_CP_MAX", "dcp_mla_decode_kernel", "DCP_MLA_KERNEL_TCGEN05", "DCP_MLA_KERNEL_MMA_SYNC"]
+           "DCP_LSE_REDUCE_CP_MAX", "dcp_mla_decode_kernel", "DCP_MLA_KERNEL_TCGEN05", "DCP_MLA_KERNEL_MMA_SYNC",
+           "dcp_mla_decode_pick_split"]
 
 
 def algorithmic_bytes(cp: int, B: int, H: int, D: int, elem: int = 2, skipped_payload_rows: int = 0) -> int:
@@ -97,19 +99,27 @@ def merge(srcs, lses, lse_base_e: bool, *, outs=None, lse_outs=None, flags: int 
     return outs, lse_outs
 
 
-def mla_decode_partial(q, kv, kv_len, scale: float, *, lse_base_e: bool = True, n_split: int = 1, dv: int = 512,
-                       outs=None, lses=None, status=None, flags: int = 0, stream=None):
+def _num_sms(device) -> int:
+    import torch
+    return int(torch.cuda.get_device_properties(device).multi_processor_count)
+
+
+def mla_decode_partial(q, kv, kv_len, scale: float, *, lse_base_e: bool = True, n_split: int | None = 1,
+                       dv: int = 512, outs=None, lses=None, status=None, flags: int = 0, stream=None):
     """Split-KV MLA decode attention over one shard with the CUDA kernel.
 
     q: CUDA bf16 [B, H, Dk]; kv: CUDA bf16 [B, T, Dk] (row b's shard-local
     tokens); kv_len: CUDA int32 [B]. Returns (outs, lses): n_split bf16
     [B, H, dv] partial outputs and n_split fp32 [B, H] LSEs, one per contiguous
-    token range of each row.
+    token range of each row. n_split=None picks a one-wave split count
+    (dcp_mla_decode_pick_split).
     """
     import torch
 
     B, H, Dk = q.shape
     T = kv.shape[1]
+    if n_split is None:
+        n_split = dcp_mla_decode_pick_split(1, B, H, T, _num_sms(q.device))
     if q.dtype != torch.bfloat16 or kv.dtype != torch.bfloat16 or not (q.is_contiguous() and kv.is_contiguous()):
         raise ValueError("q and kv must be contiguous bf16 CUDA tensors")
     if kv.shape[0] != B or kv.shape[2] != Dk or kv_len.dtype != torch.int32 or kv_len.shape != (B,):
@@ -123,19 +133,23 @@ def mla_decode_partial(q, kv, kv_len, scale: float, *, lse_base_e: bool = True, 
     return outs, lses
 
 
-def mla_decode_dcp(q, kvs, kv_lens, scale: float, *, n_split: int = 1, lse_base_e: bool = True, dv: int = 512,
-                   workspace=None, outs=None, lse_outs=None, status=None, flags: int = 0, stream=None):
+def mla_decode_dcp(q, kvs, kv_lens, scale: float, *, n_split: int | None = 1, lse_base_e: bool = True,
+                   dv: int = 512, workspace=None, outs=None, lse_outs=None, status=None, flags: int = 0,
+                   stream=None):
     """DCP decode attention on one GPU: the producer over each shard in
     ``kvs`` (bf16 [B, T, Dk] each, token counts ``kv_lens`` int32 [B] each),
     then the merge into cp destinations. Returns (outs, lse_outs): cp bf16
     [B, H/cp, dv] and cp fp32 [B, H/cp]. The workspace (a uint8 CUDA tensor of
     at least dcp_mla_decode_workspace_bytes bytes) is allocated with torch
-    when not given."""
+    when not given. n_split=None picks a one-wave split count
+    (dcp_mla_decode_pick_split)."""
     import torch
 
     cp = len(kvs)
     B, H, Dk = q.shape
     T = kvs[0].shape[1]
+    if n_split is None:
+        n_split = dcp_mla_decode_pick_split(cp, B, H, T, _num_sms(q.device))
     need = dcp_mla_decode_workspace_bytes(cp, n_split, B, H, dv)
     if workspace is None:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)

@@ -24,7 +24,7 @@ DCP_FLAG_LSE_FIRST = 4
 
 EXPORTED_SYMBOLS = ("dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dcp_lse_reduce_version",
                     "dcp_mla_decode_partial", "dcp_mla_decode_smem_bytes", "dcp_mla_decode_workspace_bytes",
-                    "dcp_mla_decode", "dcp_mla_decode_noalloc", "dcp_mla_decode_kernel")
+                    "dcp_mla_decode", "dcp_mla_decode_noalloc", "dcp_mla_decode_kernel", "dcp_mla_decode_pick_split")
 DCP_MLA_NOALLOC_SCRATCH_BYTES = 32 << 20
 DCP_MLA_SPLIT_MAX = 16
 DCP_MLA_FLAG_MMA_SYNC = 2
@@ -97,6 +97,8 @@ def load(path: str | None = None):
         lib.dcp_mla_decode_smem_bytes.restype = ci
         lib.dcp_mla_decode_kernel.argtypes = [ci, i64, ci, ctypes.c_uint]
         lib.dcp_mla_decode_kernel.restype = ci
+        lib.dcp_mla_decode_pick_split.argtypes = [ci, i64, ci, i64, ci]
+        lib.dcp_mla_decode_pick_split.restype = ci
         lib.dcp_mla_decode_workspace_bytes.argtypes = [ci, ci, i64, ci, ci]
         lib.dcp_mla_decode_workspace_bytes.restype = i64
         lib.dcp_mla_decode.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ci, i64, ci, ci, ci, i64,
@@ -189,6 +191,14 @@ def dcp_mla_decode_partial(q, kv, kv_len, B: int, H: int, Dk: int, Dv: int, T: i
 
 def dcp_mla_decode_smem_bytes(Dk: int, H: int) -> int:
     return int(load().dcp_mla_decode_smem_bytes(int(Dk), int(H)))
+
+
+def dcp_mla_decode_pick_split(cp: int, B: int, H: int, T: int, num_sms: int) -> int:
+    """A one-wave split count for cp shards (see the C header; host only)."""
+    n = int(load().dcp_mla_decode_pick_split(int(cp), int(B), int(H), int(T), int(num_sms)))
+    if n < 0:
+        _check(n)
+    return n
 
 
 def dcp_mla_decode_kernel(H: int, T: int, n_split: int, flags: int = 0) -> int:

@@ -923,6 +923,20 @@ extern "C" int dcp_mla_decode_kernel(int H, int64_t T, int n_split, unsigned fla
     return tc_is_default(H, (T + n_split - 1) / n_split) ? DCP_MLA_KERNEL_TCGEN05 : DCP_MLA_KERNEL_MMA_SYNC;
 }
 
+extern "C" int dcp_mla_decode_pick_split(int cp, int64_t B, int H, int64_t T, int num_sms) {
+    if (B < 0 || B > 65535 || T < 0 || H < 16 || H % 16 != 0 || num_sms < 1) return DCP_MLA_ERR_BAD_SHAPE;
+    if (cp < 1 || cp > DCP_MLA_SPLIT_MAX || H % cp != 0) return DCP_MLA_ERR_BAD_CP;
+    const int64_t blocks = H % 64 == 0 ? H / 64 : (H % 32 == 0 ? H / 32 : H / 16);  // head blocks per row
+    const int64_t per_split = (int64_t)cp * blocks * (B > 0 ? B : 1);                // CTAs per split count
+    int best = 1;
+    for (int n = 2; n * cp <= DCP_MLA_SPLIT_MAX; ++n) {
+        if (per_split * n > num_sms) break;                  // one wave at most
+        if ((T + n - 1) / n < kTcTok) break;                 // at least one 128-token tile per split
+        if (H % (cp * n) == 0) best = n;                     // the fused merge needs H / (cp * n) heads per source
+    }
+    return best;
+}
+
 namespace {
 
 // Validate and launch the producer over n_shard shards x n_split splits

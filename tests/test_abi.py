@@ -178,3 +178,28 @@ def test_producer_kernel_choice(lib):
     # the shared-memory query covers the larger (tcgen05) kernel
     assert dcp.dcp_mla_decode_smem_bytes(576, 64) == 224256  # 144 KB tile + 72 KB Q + misc + alignment
     assert dcp.dcp_mla_decode_smem_bytes(500, 64) == -1 and dcp.dcp_mla_decode_smem_bytes(576, 20) == -1
+
+
+def test_split_count_pick(lib):
+    """One wave of CTAs, at least one 128-token tile per split, H a multiple
+    of cp*n_split, cp*n_split <= 16 (host only)."""
+    pick = dcp.dcp_mla_decode_pick_split
+    # DeepSeek-like fused decode: 8 shards x 2 head blocks x 8 rows = 128 CTAs per split count
+    assert pick(8, 8, 128, 512, 152) == 1
+    # Kimi-like: 4 shards x 1 head block x 8 rows = 32 CTAs per split count -> 4 (128 CTAs; 16 / cp = 4)
+    assert pick(4, 8, 64, 1024, 152) == 4
+    # one shard, 8 rows x 2 blocks = 16 CTAs per split: 9 fit a wave but 128 % 9 != 0 -> 8
+    assert pick(1, 8, 128, 4096, 152) == 8
+    # short caches cap the split count at one tile per split
+    assert pick(1, 1, 128, 300, 152) == 2 and pick(1, 1, 128, 100, 152) == 1
+    # a batch that already fills the GPU gets one split
+    assert pick(1, 200, 64, 1 << 16, 152) == 1
+    # every pick is a valid producer / fused split count
+    for cp, B, H, T in [(1, 1, 16, 1 << 16), (2, 3, 96, 5000), (8, 1, 128, 32768), (16, 1, 256, 1 << 20)]:
+        n = pick(cp, B, H, T, 152)
+        assert 1 <= n and cp * n <= 16 and H % (cp * n) == 0
+    for args, status in [((0, 8, 128, 512, 152), -107), ((3, 8, 128, 512, 152), -107), ((17, 8, 272, 512, 152), -107),
+                         ((1, 8, 20, 512, 152), -102), ((1, -1, 128, 512, 152), -102), ((1, 8, 128, 512, 0), -102)]:
+        with pytest.raises(dcp.DcpError) as e:
+            pick(*args)
+        assert e.value.status == status

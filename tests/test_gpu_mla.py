@@ -353,3 +353,21 @@ def test_default_call_runs_the_kernel_the_query_names(H, T, n_split):
     c_o, _ = dcp.mla_decode_partial(dev_bf16(q), dev_bf16(kv), lens, MLA_SCALE, n_split=n_split, flags=other)
     torch.cuda.synchronize()
     assert any(not torch.equal(a_o[s], c_o[s]) for s in range(n_split))
+
+
+def test_picked_split_count_in_the_python_wrappers():
+    """n_split=None picks dcp_mla_decode_pick_split's count; the results equal
+    those of the explicit count, bit for bit."""
+    B, H, T, cp = 4, 64, 1024, 2
+    q, kv = make_mla_inputs(B, H, cp * T, 576, seed=5)
+    kvs = [dev_bf16(kv[:, j * T:(j + 1) * T]) for j in range(cp)]
+    lens = [torch.full((B,), T, dtype=torch.int32, device="cuda") for _ in range(cp)]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = dcp.dcp_mla_decode_pick_split(cp, B, H, T, sms)
+    assert n > 1
+    a, al = dcp.mla_decode_dcp(dev_bf16(q), kvs, lens, MLA_SCALE, n_split=None)
+    b, bl = dcp.mla_decode_dcp(dev_bf16(q), kvs, lens, MLA_SCALE, n_split=n)
+    po, pl = dcp.mla_decode_partial(dev_bf16(q), kvs[0], lens[0], MLA_SCALE, n_split=None)
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(a, b)) and all(torch.equal(x, y) for x, y in zip(al, bl))
+    assert len(po) == dcp.dcp_mla_decode_pick_split(1, B, H, T, sms)
