@@ -82,7 +82,7 @@ KERNELS = [dcp.DCP_MLA_FLAG_TCGEN05, dcp.DCP_MLA_FLAG_MMA_SYNC]
 @pytest.mark.parametrize("kflags", KERNELS)
 @pytest.mark.parametrize("H,Dk,T,n_split", [(16, 576, 100, 1), (64, 576, 257, 3), (128, 576, 96, 2),
                                             (32, 512, 64, 1), (16, 512, 33, 16), (64, 576, 700, 2),
-                                            (64, 512, 300, 1)])
+                                            (64, 512, 300, 1), (96, 576, 400, 1), (192, 576, 260, 1)])
 @pytest.mark.parametrize("base_e", [True, False])
 def test_partials_match_oracle(oracle_mod, H, Dk, T, n_split, base_e, kflags):
     B = 4
