@@ -664,26 +664,29 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
                     for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            // per-head maximum over the tile's tokens
-            {
+            // The running max moves only when some head's tile max exceeds it by more
+            // than 2^8, i.e. when some score does: each thread checks its own, and only
+            // then (rarely, after the first tile) are the exact tile maxima reduced.
+            bool over = false;
+#pragma unroll
+            for (int h = 0; h < kHW; h += 4) {
+                const float4 mv = *reinterpret_cast<const float4*>(m_s + hb + h);
+                over |= (sv[h] > mv.x + 8.f) | (sv[h + 1] > mv.y + 8.f) | (sv[h + 2] > mv.z + 8.f) |
+                        (sv[h + 3] > mv.w + 8.f);
+            }
+            const int any = __syncthreads_or(over);
+            if (any) {
                 float mx[kHW];
 #pragma unroll
                 for (int h = 0; h < kHW; ++h) mx[h] = sv[h];
                 cta_reduce_heads<kNH, kHW, false>(mx, quad, hb, lane, red, t_s);
-            }
-            // move the running max only when some head's tile max exceeds it by more than 2^8
-            const bool need = tid < kNH && t_s[tid] > m_s[tid] + 8.f;
-            const int any = __syncthreads_or(need);
-            if (tid < kNH) {
-                if (any) {
+                if (tid < kNH) {
                     const float mn = fmaxf(m_s[tid], t_s[tid]);
                     a_s[tid] = ex2(m_s[tid] - mn);
                     m_s[tid] = mn;
-                } else {
-                    a_s[tid] = 1.f;
                 }
+                __syncthreads();
             }
-            __syncthreads();
             if (any && i > 0) {  // rescale O^T (the previous tile's value MMAs are done)
                 mbar_wait(bar_o, (uint32_t)((i - 1) & 1), p.status);
                 tc_fence_after();
