@@ -926,6 +926,14 @@ extern "C" int dcp_mla_decode_kernel(int H, int64_t T, int n_split, unsigned fla
     return tc_is_default(H, (T + n_split - 1) / n_split) ? DCP_MLA_KERNEL_TCGEN05 : DCP_MLA_KERNEL_MMA_SYNC;
 }
 
+// CTAs of the mma.sync kernel that fit on one SM (shared memory bound, Dk = 576)
+static int mma_ctas_per_sm(int H) {
+    constexpr int kSmemPerSm = 228 * 1024, kReserve = 1024;
+    const int bytes = H % 64 == 0 ? smem_bytes<576, 4>() : (H % 32 == 0 ? smem_bytes<576, 2>() : smem_bytes<576, 1>());
+    const int n = kSmemPerSm / (bytes + kReserve);
+    return n > 0 ? n : 1;
+}
+
 extern "C" int dcp_mla_decode_pick_split(int cp, int64_t B, int H, int64_t T, int num_sms) {
     if (B < 0 || B > 65535 || T < 0 || H < 16 || H % 16 != 0 || num_sms < 1) return DCP_MLA_ERR_BAD_SHAPE;
     if (cp < 1 || cp > DCP_MLA_SPLIT_MAX || H % cp != 0) return DCP_MLA_ERR_BAD_CP;
@@ -933,8 +941,11 @@ extern "C" int dcp_mla_decode_pick_split(int cp, int64_t B, int H, int64_t T, in
     const int64_t per_split = (int64_t)cp * blocks * (B > 0 ? B : 1);                // CTAs per split count
     int best = 1;
     for (int n = 2; n * cp <= DCP_MLA_SPLIT_MAX; ++n) {
-        if (per_split * n > num_sms) break;                  // one wave at most
-        if ((T + n - 1) / n < kTcTok) break;                 // at least one 128-token tile per split
+        const int64_t tokens = (T + n - 1) / n;
+        if (tokens < kTcTok) break;                          // at least one 128-token tile per split
+        // one wave: one tcgen05 CTA per SM, or as many mma.sync CTAs as fit
+        const int64_t wave = (int64_t)num_sms * (tc_is_default(H, tokens) ? 1 : mma_ctas_per_sm(H));
+        if (per_split * n > wave) continue;
         if (H % (cp * n) == 0) best = n;                     // the fused merge needs H / (cp * n) heads per source
     }
     return best;

@@ -118,7 +118,8 @@ int dcp_mla_decode_kernel(int H, int64_t T, int n_split, unsigned flags);
  * A split count for cp shards of B rows, H heads and T cache tokens per row on
  * a GPU with num_sms multiprocessors (cudaDevAttrMultiProcessorCount): the
  * largest n_split with cp*n_split <= DCP_MLA_SPLIT_MAX whose producer launch
- * (cp * n_split * head blocks * B CTAs, one per SM) fits in one wave, whose
+ * (cp * n_split * head blocks * B CTAs; one per SM for the tcgen05 kernel, as
+ * many as fit for the mma.sync kernel) fits in one wave, whose
  * splits hold at least one 128-token tile (ceil(T / n_split) >= 128), and
  * with H a multiple of cp*n_split (as dcp_mla_decode needs); 1 when no larger
  * count qualifies. Use cp = 1 for a single dcp_mla_decode_partial call. Host

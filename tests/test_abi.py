@@ -194,6 +194,8 @@ def test_split_count_pick(lib):
     assert pick(1, 1, 128, 300, 152) == 2 and pick(1, 1, 128, 100, 152) == 1
     # a batch that already fills the GPU gets one split
     assert pick(1, 200, 64, 1 << 16, 152) == 1
+    # 16-head blocks run on the mma.sync kernel, two CTAs per SM: a wave holds 304 of them
+    assert pick(1, 148, 16, 4096, 152) == 2 and pick(1, 64, 16, 2048, 152) == 4
     # every pick is a valid producer / fused split count
     for cp, B, H, T in [(1, 1, 16, 1 << 16), (2, 3, 96, 5000), (8, 1, 128, 32768), (16, 1, 256, 1 << 20)]:
         n = pick(cp, B, H, T, 152)
