@@ -23,12 +23,14 @@
 //
 // Two schedules, chosen per call:
 //   PRELOAD    one unit per warp; the payload loads are issued together with
-//              the LSE loads (one memory round trip). Used when every warp of
-//              the grid fits on the GPU at once: small batches, latency-bound.
+//              the LSE loads (one memory round trip), in as many waves of CTAs
+//              as the batch needs. The default for D = 512 and cp <= 8.
 //   LSE_FIRST  persistent grid (one wave of CTAs); a warp strides over units,
 //              reads the next unit's LSEs while the current payload is in
 //              flight, and issues payload loads only for sources of nonzero
-//              weight, so empty shards cost no payload bytes.
+//              weight, so empty shards cost no payload bytes. Used for other
+//              shapes, and with seq_lens masking when the grid would not fit
+//              in one resident wave.
 // Both give bit-identical results.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -493,12 +495,15 @@ cudaError_t launch_cp(const Launch& L) {
         const int rows = (int)((L.B - b0) < rows_per_launch ? (L.B - b0) : rows_per_launch);
         const int64_t units = (int64_t)rows * L.H;
         // One unit per warp with the payload loads issued beside the LSE loads
-        // when every warp of the grid is resident at once; otherwise one
-        // persistent wave that reads LSEs a unit ahead and skips empty sources.
+        // (in as many waves as it takes) is the faster stream whenever it is
+        // available. The persistent wave that reads LSEs a unit ahead and skips
+        // empty sources is kept for seq_lens masking on grids larger than one
+        // resident wave, where skipping the masked payloads pays.
         bool preload = false;
         if constexpr (kCanPreload) {
             const int threads = units <= 1024 ? 64 : 128;
-            preload = units <= (int64_t)L.sms * occupancy<kF16, kMaxCp, kFixedChunks, true>(threads) * (threads / 32);
+            preload = L.seq_lens == nullptr ||
+                      units <= (int64_t)L.sms * occupancy<kF16, kMaxCp, kFixedChunks, true>(threads) * (threads / 32);
         }
         if (L.flags & DCP_FLAG_PRELOAD) preload = kCanPreload;
         if (L.flags & DCP_FLAG_LSE_FIRST) preload = false;
