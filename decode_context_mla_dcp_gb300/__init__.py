@@ -15,6 +15,7 @@ from torch tensors and allocates the outputs.
 from __future__ import annotations
 
 from ._binding import (DCP_DTYPE_BF16, DCP_DTYPE_F16, DCP_FLAG_LSE_FIRST, DCP_FLAG_PDL, DCP_FLAG_PRELOAD,
+                       DCP_FLAG_PREFETCH,
                        DCP_LSE_REDUCE_CP_MAX, DCP_MLA_FLAG_MMA_SYNC, DCP_MLA_FLAG_TCGEN05, DCP_MLA_SPLIT_MAX,
                        DCP_MLA_KERNEL_MMA_SYNC, DCP_MLA_KERNEL_TCGEN05, dcp_mla_decode_kernel,
                        dcp_mla_decode_pick_split,
@@ -31,6 +32,7 @@ __all__ = ["dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dc
            "DCP_MLA_NOALLOC_SCRATCH_BYTES", "DCP_MLA_FLAG_MMA_SYNC", "DCP_MLA_FLAG_TCGEN05",
            "algorithmic_bytes", "Layout", "DcpError", "load", "library_path", "EXPORTED_SYMBOLS",
            "DCP_DTYPE_BF16", "DCP_DTYPE_F16", "DCP_FLAG_PDL", "DCP_FLAG_PRELOAD", "DCP_FLAG_LSE_FIRST",
+           "DCP_FLAG_PREFETCH",
            "DCP_LSE_REDUCE_CP_MAX", "dcp_mla_decode_kernel", "DCP_MLA_KERNEL_TCGEN05", "DCP_MLA_KERNEL_MMA_SYNC",
            "dcp_mla_decode_pick_split"]
 

@@ -21,6 +21,7 @@ DCP_DTYPE_F16 = 1
 DCP_FLAG_PDL = 1
 DCP_FLAG_PRELOAD = 2
 DCP_FLAG_LSE_FIRST = 4
+DCP_FLAG_PREFETCH = 8
 
 EXPORTED_SYMBOLS = ("dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dcp_lse_reduce_version",
                     "dcp_mla_decode_partial", "dcp_mla_decode_smem_bytes", "dcp_mla_decode_workspace_bytes",
@@ -31,16 +32,6 @@ DCP_MLA_FLAG_MMA_SYNC = 2
 DCP_MLA_FLAG_TCGEN05 = 4
 DCP_MLA_KERNEL_TCGEN05 = 1
 DCP_MLA_KERNEL_MMA_SYNC = 2
-_MLA_ERRORS = {-101: "q, kv, kv_len, out_ptrs, lse_ptrs or an entry is NULL",
-               -102: "B must be in [0, 65535], T >= 0, H a positive multiple of 16, Dk 512 or 576, Dv 512",
-               -103: "n_split must be in [1, 16]",
-               -104: "q, kv and outputs must be 16-byte aligned; LSE, kv_len and status 4-byte aligned",
-               -105: "unknown flag bits, or DCP_MLA_FLAG_MMA_SYNC together with DCP_MLA_FLAG_TCGEN05",
-               -106: "workspace is NULL, not 256-byte aligned, or smaller than dcp_mla_decode_workspace_bytes",
-               -107: "cp*n_split must be <= 16 and divide H",
-               -108: "the partials need more than the built-in 32 MiB scratch (DCP_MLA_NOALLOC_SCRATCH_BYTES)",
-               -109: "the built-in scratch array's device address could not be obtained on this device",
-               -110: "a TMA tensor map for q or a cache could not be encoded"}
 DCP_LSE_REDUCE_INTERLEAVE_MAX = 1 << 24
 
 
@@ -173,8 +164,6 @@ def dcp_lse_reduce_ex(src_ptrs, lse_ptrs, cp: int, B: int, H: int, D: int, lse_b
 
 
 def dcp_lse_reduce_strerror(status: int) -> str:
-    if int(status) in _MLA_ERRORS:
-        return _MLA_ERRORS[int(status)]
     return load().dcp_lse_reduce_strerror(int(status)).decode()
 
 

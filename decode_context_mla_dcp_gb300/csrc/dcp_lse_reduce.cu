@@ -39,6 +39,7 @@
 #include <stdint.h>
 
 #include "dcp_lse_reduce.h"
+#include "dcp_mla_decode.h"
 
 namespace {
 
@@ -59,6 +60,7 @@ struct Params {
     float lse_scale;              // turns LSE differences into log2 units: 1 or log2(e)
     float log_scale;              // turns log2(sum) into the LSE base: 1 or ln(2)
     int interleave;               // KV tokens per interleave block (with seq_lens)
+    int prefetch_first;           // 1: warm L2 with the first unit's inputs before the dependency wait
     const int* seq_lens;          // per-row context length, or null: no masking
     int64_t lse_row, lse_head;    // elements
     int64_t src_row, src_head;    // elements
@@ -126,6 +128,15 @@ __device__ __forceinline__ int ld_nc_s32(const int* ptr) {
     int v;
     asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(ptr));
     return v;
+}
+
+// L2 prefetches: hints with no effect on the values later loads return. The
+// bulk form covers `bytes` (a multiple of 16) from a 16-byte aligned address.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2_line(const void* ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr) : "memory");
 }
 
 __device__ __forceinline__ void st_v4(uint8_t* ptr, const uint4& v) {
@@ -283,6 +294,20 @@ __device__ __forceinline__ int64_t src_offset(const Params<kMaxCp>& p, const Pos
     return ((int64_t)q.b * p.src_row + (int64_t)(q.r * p.Hl + q.i) * p.src_head) * 2;  // bytes
 }
 
+// Bring one unit's inputs into L2: lane j < cp takes source j's row (D*2
+// bytes, one bulk prefetch), lane 16 + j its LSE line, lane 31 the row's
+// context length.
+template <int kMaxCp>
+__device__ __forceinline__ void prefetch_unit(const Params<kMaxCp>& p, const Pos& q, int lane) {
+    if (lane < p.cp) {
+        prefetch_l2_bulk(p.src[lane] + src_offset(p, q), (uint32_t)p.D * 2u);
+    } else if (lane >= 16 && lane - 16 < p.cp) {
+        prefetch_l2_line(p.lse[lane - 16] + (int64_t)q.b * p.lse_row + (int64_t)(q.r * p.Hl + q.i) * p.lse_head);
+    } else if (lane == 31 && p.seq_lens != nullptr) {
+        prefetch_l2_line(p.seq_lens + q.b);
+    }
+}
+
 // ---- the kernel ----------------------------------------------------------------
 
 // Register budget for D = 512: keep 7 CTAs of 4 warps resident per SM for up
@@ -329,6 +354,11 @@ __global__ void __launch_bounds__(kMaxThreads, min_ctas_per_sm<kMaxCp, kFixedChu
             asm volatile("" : "+l"(sp[j]));
         }
     }
+
+    // A prefetch only warms L2 (the point of coherence), so it may run before
+    // the wait: if the previous kernel writes these inputs, the loads after the
+    // wait still see its values.
+    if (p.prefetch_first) prefetch_unit(p, q, lane);
 
     // Inputs may come from the previous kernel in the stream (PDL): wait for it
     // before the first load. Then let the next kernel start its launch.
@@ -399,6 +429,7 @@ __global__ void __launch_bounds__(kMaxThreads, min_ctas_per_sm<kMaxCp, kFixedChu
     }
 }
 
+
 // ---- host side -----------------------------------------------------------------
 
 // Everything a launch needs, independent of the source count.
@@ -439,23 +470,25 @@ int occupancy(int threads) {
     return ctas_per_sm(lse_merge_kernel<kF16, kMaxCp, kFixedChunks, kPreload>, threads, cache);
 }
 
-template <bool kF16, int kMaxCp, int kFixedChunks, bool kPreload>
-cudaError_t launch_one(const Launch& L, int64_t b0, int rows, int threads, int ctas) {
+// The parameters of one launch over rows [b0, b0 + rows), `step` warps apart.
+template <int kMaxCp>
+Params<kMaxCp> make_params(const Launch& L, int64_t b0, int rows, int step) {
     Params<kMaxCp> p;
-    const int H = L.H, Hl = L.H / L.cp, wpc = threads / 32;
+    const int H = L.H, Hl = L.H / L.cp;
     p.units = rows * H;
     p.H = H;
     p.Hl = Hl;
     p.cp = L.cp;
     p.D = L.D;
-    p.step = ctas * wpc;
-    p.step_b = p.step / H;
-    const int sh = p.step % H;
+    p.step = step;
+    p.step_b = step / H;
+    const int sh = step % H;
     p.step_r = sh / Hl;
     p.step_i = sh % Hl;
     p.lse_scale = L.base_e ? 1.4426950408889634f : 1.0f;
     p.log_scale = L.base_e ? 0.6931471805599453f : 1.0f;
     p.interleave = L.interleave;
+    p.prefetch_first = (L.flags & DCP_FLAG_PREFETCH) ? 1 : 0;
     p.seq_lens = L.seq_lens != nullptr ? L.seq_lens + b0 : nullptr;
     p.lse_row = L.lay.lse_row;
     p.lse_head = L.lay.lse_head;
@@ -472,17 +505,28 @@ cudaError_t launch_one(const Launch& L, int64_t b0, int rows, int threads, int c
         float* lo = (on && L.lse_out != nullptr) ? L.lse_out[j] : nullptr;
         p.lse_out[j] = lo != nullptr ? lo + b0 * L.lay.lse_out_row : nullptr;
     }
+    return p;
+}
+
+template <typename K, typename P>
+cudaError_t launch_kernel(const Launch& L, K kernel, const P& p, int ctas, int threads, int smem) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas, 1, 1);
     cfg.blockDim = dim3((unsigned)threads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (L.flags & DCP_FLAG_PDL) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<kF16, kMaxCp, kFixedChunks, kPreload>, p);
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+template <bool kF16, int kMaxCp, int kFixedChunks, bool kPreload>
+cudaError_t launch_one(const Launch& L, int64_t b0, int rows, int threads, int ctas) {
+    const Params<kMaxCp> p = make_params<kMaxCp>(L, b0, rows, ctas * (threads / 32));
+    return launch_kernel(L, lse_merge_kernel<kF16, kMaxCp, kFixedChunks, kPreload>, p, ctas, threads, 0);
 }
 
 // Pick the schedule and grid for one instantiation family and launch every
@@ -556,7 +600,8 @@ extern "C" int dcp_lse_reduce_ex(const void* const* src_ptrs, const float* const
     if (H % cp != 0) return DCP_ERR_HEADS_NOT_DIVISIBLE;
     if (dtype != DCP_DTYPE_BF16 && dtype != DCP_DTYPE_F16) return DCP_ERR_BAD_DTYPE;
     if (lse_base_e != 0 && lse_base_e != 1) return DCP_ERR_BAD_BASE;
-    if ((flags & ~(DCP_FLAG_PDL | DCP_FLAG_PRELOAD | DCP_FLAG_LSE_FIRST)) != 0) return DCP_ERR_BAD_FLAGS;
+    if ((flags & ~(DCP_FLAG_PDL | DCP_FLAG_PRELOAD | DCP_FLAG_LSE_FIRST | DCP_FLAG_PREFETCH)) != 0)
+        return DCP_ERR_BAD_FLAGS;
     if ((flags & DCP_FLAG_PRELOAD) && (flags & DCP_FLAG_LSE_FIRST)) return DCP_ERR_BAD_FLAGS;
     if (seq_lens != nullptr) {
         if (interleave < 1 || interleave > DCP_LSE_REDUCE_INTERLEAVE_MAX) return DCP_ERR_BAD_INTERLEAVE;
@@ -657,6 +702,22 @@ extern "C" const char* dcp_lse_reduce_strerror(int status) {
         case DCP_ERR_BAD_BASE: return "lse_base_e must be 0 (base 2) or 1 (base e)";
         case DCP_ERR_DEVICE: return "could not query the current CUDA device";
         case DCP_ERR_BAD_INTERLEAVE: return "interleave must be in [1, 2^24] when seq_lens is given";
+        // the producer and the fused decode (include/dcp_mla_decode.h)
+        case DCP_MLA_ERR_NULL_POINTER: return "q, kv, kv_len, out_ptrs, lse_ptrs or an entry is NULL";
+        case DCP_MLA_ERR_BAD_SHAPE:
+            return "B must be in [0, 65535], T >= 0, H a positive multiple of 16, Dk 512 or 576, Dv 512";
+        case DCP_MLA_ERR_BAD_SPLIT: return "n_split must be in [1, 16]";
+        case DCP_MLA_ERR_MISALIGNED:
+            return "q, kv and outputs must be 16-byte aligned; LSE, kv_len and status 4-byte aligned";
+        case DCP_MLA_ERR_BAD_FLAGS: return "unknown flag bits, or DCP_MLA_FLAG_MMA_SYNC together with DCP_MLA_FLAG_TCGEN05";
+        case DCP_MLA_ERR_WORKSPACE:
+            return "workspace is NULL, not 256-byte aligned, or smaller than dcp_mla_decode_workspace_bytes";
+        case DCP_MLA_ERR_BAD_CP: return "cp*n_split must be <= 16 and divide H";
+        case DCP_MLA_ERR_SCRATCH_LIMIT:
+            return "the partials need more than the built-in 32 MiB scratch (DCP_MLA_NOALLOC_SCRATCH_BYTES)";
+        case DCP_MLA_ERR_SCRATCH_SETUP:
+            return "the built-in scratch array's device address could not be obtained on this device";
+        case DCP_MLA_ERR_TENSOR_MAP: return "a TMA tensor map for q or a cache could not be encoded";
         default: break;
     }
     if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));

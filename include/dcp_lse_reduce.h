@@ -29,8 +29,13 @@
  *
  * Numerics. Weights and accumulation in fp32, sources taken in order
  * j = 0..cp-1, output rounded to bf16/fp16 (round to nearest even). A source
- * whose weight is 0 (LSE = -inf, or underflow) is neither read nor added, so
- * a NaN payload behind a -inf LSE does not leak. A (row, head) whose every
+ * whose weight is 0 (LSE = -inf, or underflow) is never added, so a NaN
+ * payload behind a -inf LSE does not leak. Whether its payload is read
+ * depends on the schedule: the default one-(row, head)-per-warp schedule
+ * issues every payload load together with the LSE loads (one memory round
+ * trip) and drops zero-weight rows before the sum; DCP_FLAG_LSE_FIRST, and
+ * seq_lens masking on grids of more than one resident wave, read the LSEs
+ * first and never read a zero-weight payload. A (row, head) whose every
  * source is -inf gives an output of 0 and a merged LSE of -inf. The result
  * is bit-identical across calls, launch schedules and graph replays.
  *
@@ -73,6 +78,12 @@ extern "C" {
                                   for D = 512 and cp <= 8; ignored otherwise) */
 #define DCP_FLAG_LSE_FIRST 4u  /* force the persistent schedule that reads the
                                   LSEs first and skips zero-weight payloads */
+#define DCP_FLAG_PREFETCH 8u   /* each warp brings its first (row, head)'s inputs
+                                  into L2 before it waits for the previous kernel
+                                  (with DCP_FLAG_PDL: that wait overlaps the
+                                  previous kernel's tail). A hint: the values read
+                                  are the same; if the previous kernel writes these
+                                  inputs, the prefetch only adds reads */
 
 enum {
     DCP_OK = 0,
@@ -147,7 +158,8 @@ typedef struct dcp_lse_reduce_layout {
  *               (t / interleave) % cp), so shard j owns a token of a context
  *               of L tokens iff L > j*interleave. A shard that owns none is
  *               empty for that row: its LSE entry is ignored (it may hold
- *               anything) and its payload is neither read nor added. L = 0
+ *               anything) and its payload is never added (nor read, under
+ *               the schedule that reads LSEs first; see Numerics). L = 0
  *               gives an output of 0 and a merged LSE of -inf.
  *   interleave  tokens per interleave block, 1..DCP_LSE_REDUCE_INTERLEAVE_MAX
  *               (read only when seq_lens is given).

@@ -95,8 +95,10 @@ def test_ex_rejects_bad_flags_dtype_strides(lib):
 
     assert ex(dtype=2) == -8
     assert ex(base_e=2) == -9
-    assert ex(flags=8) == -7
+    assert ex(flags=32) == -7
     assert ex(flags=dcp.DCP_FLAG_PRELOAD | dcp.DCP_FLAG_LSE_FIRST) == -7
+    assert ex(flags=16) == -7
+    assert ex(flags=dcp.DCP_FLAG_PRELOAD | dcp.DCP_FLAG_LSE_FIRST | dcp.DCP_FLAG_PREFETCH) == -7
     assert ex(seq_lens=FAKE, interleave=0) == -11
     assert ex(seq_lens=FAKE, interleave=(1 << 24) + 1) == -11
     assert ex(seq_lens=FAKE + 2, interleave=1) == -6
@@ -132,6 +134,18 @@ def test_mla_producer_rejects_bad_arguments(lib):
     assert call(B=0) == 0  # nothing to do, nothing launched
     assert dcp.dcp_mla_decode_smem_bytes(576, 64) > 150000
     assert "n_split" in dcp.dcp_lse_reduce_strerror(-103)
+
+
+def test_every_status_code_has_a_message_in_the_c_library(lib):
+    # The producer's and the fused decode's codes are explained by the C
+    # library itself, so a C caller needs no table of its own.
+    lib.dcp_lse_reduce_strerror.restype = ctypes.c_char_p
+    assert b"n_split" in lib.dcp_lse_reduce_strerror(-103)
+    for code in list(range(-11, 0)) + list(range(-110, -100)):
+        msg = lib.dcp_lse_reduce_strerror(code)
+        assert msg and msg != b"unknown status", code
+    assert lib.dcp_lse_reduce_strerror(-12) == b"unknown status"
+    assert lib.dcp_lse_reduce_strerror(-100) == b"unknown status"
 
 
 def test_fused_decode_rejects_bad_workspace_and_cp(lib):

@@ -247,6 +247,45 @@ def test_lse_stride_and_null_lse_outputs(oracle_mod):
     assert louts is None
 
 
+@pytest.mark.parametrize("s_q", [2, 4])
+@pytest.mark.parametrize("flags", [0, dcp.DCP_FLAG_PRELOAD, dcp.DCP_FLAG_LSE_FIRST,
+                                   dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH])
+def test_flashmla_lse_head_stride(oracle_mod, s_q, flags):
+    # FlashMLA with s_q query tokens per row: partial outputs [B, s_q, H, D],
+    # LSEs [B, H, s_q]. One call per token t: sources start t*H*D elements in
+    # with row stride s_q*H*D; LSEs start t elements in with row stride H*s_q
+    # and head stride s_q; destinations are [B, s_q, H/cp, D] and merged LSEs
+    # [B, s_q, H/cp]. Checked element by element against the oracle called
+    # with the same strides ("[DCP] Run fi_a2a on FlashInfer's fused
+    # all-to-all + LSE reduce", "Accuracy Tests": FlashMLA's LSE layout).
+    B, cp, H, D = 9, 8, 128, 512
+    Hl = H // cp
+    inp = make_merge_inputs("deepseek", B * s_q, seed=40 + s_q)
+    src_full = [s.reshape(B, s_q, H, D) for s in inp.srcs]
+    lse_full = [np.ascontiguousarray(l.reshape(B, s_q, H).transpose(0, 2, 1)) for l in inp.lses]  # [B, H, s_q]
+    srcs = [to_dev_bits(s) for s in src_full]
+    lses = [torch.from_numpy(l).cuda() for l in lse_full]
+    outs = [Guarded((B, s_q, Hl, D), torch.bfloat16) for _ in range(cp)]
+    louts = [Guarded((B, s_q, Hl), torch.float32) for _ in range(cp)]
+    lay = dcp.Layout(src_row=s_q * H * D, src_head=D, lse_row=H * s_q, lse_head=s_q,
+                     dst_row=s_q * Hl * D, dst_head=D, lse_out_row=s_q * Hl)
+    for t in range(s_q):
+        dcp.dcp_lse_reduce_ex([x.data_ptr() + t * H * D * 2 for x in srcs], [x.data_ptr() + t * 4 for x in lses],
+                              cp, B, H, D, True, dcp.DCP_DTYPE_BF16,
+                              [o.t.data_ptr() + t * Hl * D * 2 for o in outs],
+                              [o.t.data_ptr() + t * Hl * 4 for o in louts], layout=lay, flags=flags)
+    torch.cuda.synchronize()
+    for g in outs + louts:
+        assert g.guards_ok(), "a write landed outside an output buffer"
+    for t in range(s_q):
+        ref, lref = oracle_mod.merge([np.ascontiguousarray(s[:, t]) for s in src_full],
+                                     [l.reshape(-1)[t:] for l in lse_full], True, H=H, D=D,
+                                     lse_strides=(H * s_q, s_q))
+        for r in range(cp):
+            assert_out_close(outs[r].t[:, t].float().double().cpu().numpy(), ref[r], f"s_q={s_q} t={t} dest {r}")
+            assert_lse_close(louts[r].t[:, t].double().cpu().numpy(), lref[r], f"s_q={s_q} t={t} dest {r}")
+
+
 def test_strided_layouts(oracle_mod):
     # padded token stride for sources, a wider head backing array, and padded
     # destinations, through the tensor-level entry point
@@ -349,11 +388,55 @@ def test_bit_identical_across_calls_schedules_and_pdl():
     lses = [torch.from_numpy(l).cuda() for l in inp.lses]
     base_o, base_l = dcp.merge(srcs, lses, True)
     ref = _bits(base_o) + _bits(base_l)
+    pf = dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH
     for flags in [0, 0, dcp.DCP_FLAG_PRELOAD, dcp.DCP_FLAG_LSE_FIRST, dcp.DCP_FLAG_PDL,
-                  dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PRELOAD]:
+                  dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PRELOAD, pf, pf | dcp.DCP_FLAG_PRELOAD,
+                  pf | dcp.DCP_FLAG_LSE_FIRST, dcp.DCP_FLAG_PREFETCH]:
         o, l = dcp.merge(srcs, lses, True, flags=flags)
         got = _bits(o) + _bits(l)
         assert all(torch.equal(a, b) for a, b in zip(ref, got)), f"flags={flags}"
+
+
+def test_prefetch_before_the_wait_sees_the_previous_kernels_writes():
+    # Merge A writes outputs that merge B reads as its sources and LSEs. With
+    # PDL, B's CTAs start while A runs and prefetch those lines into L2 before
+    # A has written them (they hold NaN then); after its wait B must read A's
+    # values. Compared bit for bit with the same chain run without PDL or
+    # prefetch, 20 times over.
+    B, H, cp = 64, 32, 2
+    inp = make_merge_inputs("kimi", B, seed=31, cp=cp, H=H)
+    srcs = [to_dev_bits(s) for s in inp.srcs]
+    lses = [torch.from_numpy(l).cuda() for l in inp.lses]
+    mid = [torch.empty((B, H // cp, 512), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
+    mid_l = [torch.empty((B, H // cp), dtype=torch.float32, device="cuda") for _ in range(cp)]
+    fin = [torch.empty((B, H // (2 * cp), 512), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
+    fin_l = [torch.empty((B, H // (2 * cp)), dtype=torch.float32, device="cuda") for _ in range(cp)]
+
+    flush = torch.zeros((160 << 20,), dtype=torch.float32, device="cuda")  # 640 MB, more than L2
+
+    def chain(flags, evict=False):
+        for t in mid + mid_l + fin + fin_l:
+            t.fill_(float("nan"))
+        if evict:  # the NaN lines go back to DRAM, so B's prefetch brings them from there
+            flush.add_(1.0)
+        dcp.merge(srcs, lses, False, outs=mid, lse_outs=mid_l, flags=flags)
+        dcp.merge(mid, mid_l, False, outs=fin, lse_outs=fin_l, flags=flags)
+        torch.cuda.synchronize()
+        return _bits(mid) + _bits(mid_l) + _bits(fin) + _bits(fin_l)
+
+    ref = chain(0)
+    assert not any(bool(torch.isnan(t).any()) for t in fin)
+    for it in range(20):
+        flags = dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH | (dcp.DCP_FLAG_LSE_FIRST if it % 2 else 0)
+        assert all(torch.equal(a, b) for a, b in zip(ref, chain(flags, evict=it % 4 < 2))), f"iteration {it}"
+
+
+@pytest.mark.parametrize("flags", [dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH,
+                                   dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH | dcp.DCP_FLAG_LSE_FIRST,
+                                   dcp.DCP_FLAG_PREFETCH | dcp.DCP_FLAG_PRELOAD])
+@pytest.mark.parametrize("cfg,rows", [("kimi", 1), ("kimi", 128), ("kimi", 512), ("deepseek", 64)])
+def test_prefetch_flags_match_the_oracle(oracle_mod, flags, cfg, rows):
+    check_against_oracle(oracle_mod, make_merge_inputs(cfg, rows, seed=7), flags=flags, what=f"{cfg} B={rows}")
 
 
 @pytest.mark.parametrize("pdl", [False, True])
