@@ -953,6 +953,11 @@ extern "C" int dcp_mla_decode_pick_split(int cp, int64_t B, int H, int64_t T, in
 
 namespace {
 
+// The shapes the producer takes (DCP_MLA_ERR_BAD_SHAPE otherwise).
+bool shape_ok(int64_t B, int H, int Dk, int Dv, int64_t T) {
+    return B >= 0 && B <= 65535 && T >= 0 && H >= 16 && H % 16 == 0 && (Dk == 512 || Dk == 576) && Dv == kDv;
+}
+
 // Validate and launch the producer over n_shard shards x n_split splits
 // (slot = shard * n_split + split), all in one grid.
 int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv_len_ptrs, int n_shard, int64_t B,
@@ -960,8 +965,7 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
              float* const* lse_ptrs, int32_t* status, unsigned flags, void* stream) {
     if (q == nullptr || kv_ptrs == nullptr || kv_len_ptrs == nullptr || out_ptrs == nullptr || lse_ptrs == nullptr)
         return DCP_MLA_ERR_NULL_POINTER;
-    if (B < 0 || B > 65535 || T < 0 || H < 16 || H % 16 != 0 || (Dk != 512 && Dk != 576) || Dv != kDv)
-        return DCP_MLA_ERR_BAD_SHAPE;
+    if (!shape_ok(B, H, Dk, Dv, T)) return DCP_MLA_ERR_BAD_SHAPE;
     if (n_split < 1 || n_split > DCP_MLA_SPLIT_MAX) return DCP_MLA_ERR_BAD_SPLIT;
     if (n_shard < 1 || n_shard * n_split > kSlots) return DCP_MLA_ERR_BAD_CP;
     if ((flags & ~(kFlagPdl | kFlagMmaSync | kFlagTcgen05)) != 0) return DCP_MLA_ERR_BAD_FLAGS;
@@ -1063,8 +1067,9 @@ extern "C" int dcp_mla_decode(const void* q, const void* const* kv_ptrs, const i
                               void* workspace, int64_t workspace_bytes, void* const* dst_ptrs,
                               float* const* lse_out_ptrs, int32_t* status, unsigned flags, void* stream) {
     if (kv_ptrs == nullptr || kv_len_ptrs == nullptr || dst_ptrs == nullptr) return DCP_MLA_ERR_NULL_POINTER;
+    if (!shape_ok(B, H, Dk, Dv, T)) return DCP_MLA_ERR_BAD_SHAPE;
     if (n_split < 1 || n_split > DCP_MLA_SPLIT_MAX) return DCP_MLA_ERR_BAD_SPLIT;
-    if (cp < 1 || cp * n_split > DCP_LSE_REDUCE_CP_MAX || H < 1 || H % (cp * n_split) != 0) return DCP_MLA_ERR_BAD_CP;
+    if (cp < 1 || cp * n_split > DCP_LSE_REDUCE_CP_MAX || H % (cp * n_split) != 0) return DCP_MLA_ERR_BAD_CP;
     const int64_t need = dcp_mla_decode_workspace_bytes(cp, n_split, B, H, Dv);
     if (need < 0) return DCP_MLA_ERR_BAD_SHAPE;
     if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) != 0 ||
@@ -1146,8 +1151,12 @@ extern "C" int dcp_mla_decode_noalloc(const void* q, const void* const* kv_ptrs,
                                       int cp, int64_t B, int H, int Dk, int Dv, int64_t T, float scale,
                                       int lse_base_e, int n_split, void* const* dst_ptrs, float* const* lse_out_ptrs,
                                       int32_t* status, unsigned flags, void* stream) {
+    // the same argument checks as dcp_mla_decode, in the same order, before the
+    // scratch limit: a bad shape reports itself, not as too large
+    if (kv_ptrs == nullptr || kv_len_ptrs == nullptr || dst_ptrs == nullptr) return DCP_MLA_ERR_NULL_POINTER;
+    if (!shape_ok(B, H, Dk, Dv, T)) return DCP_MLA_ERR_BAD_SHAPE;
     if (n_split < 1 || n_split > DCP_MLA_SPLIT_MAX) return DCP_MLA_ERR_BAD_SPLIT;
-    if (cp < 1 || cp * n_split > DCP_LSE_REDUCE_CP_MAX || H < 1 || H % (cp * n_split) != 0) return DCP_MLA_ERR_BAD_CP;
+    if (cp < 1 || cp * n_split > DCP_LSE_REDUCE_CP_MAX || H % (cp * n_split) != 0) return DCP_MLA_ERR_BAD_CP;
     const int64_t need = dcp_mla_decode_workspace_bytes(cp, n_split, B, H, Dv);
     if (need < 0) return DCP_MLA_ERR_BAD_SHAPE;
     if (need > (int64_t)DCP_MLA_NOALLOC_SCRATCH_BYTES) return DCP_MLA_ERR_SCRATCH_LIMIT;

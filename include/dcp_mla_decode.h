@@ -189,7 +189,16 @@ int dcp_mla_decode(const void* q, const void* const* kv_ptrs, const int32_t* con
  *
  * The first call on a device looks up the array's device address on that
  * device (the calling thread's current device) and keeps it; make that first
- * call outside any stream capture. The array is shared by every call on a
+ * call outside any stream capture. The array becomes resident on a device
+ * when the library's code is loaded there, which under CUDA's default lazy
+ * module loading can be this first call (or the first call of any producer
+ * entry point): that is when the 32 MiB are committed, and if the device has
+ * no free memory left by then the call returns DCP_MLA_ERR_SCRATCH_SETUP. So
+ * make one warm-up call per device during initialisation, before other
+ * allocators reserve the device's memory; a call with B = 0 and otherwise
+ * valid arguments launches nothing and does only this set-up. Argument errors
+ * are reported as by dcp_mla_decode (a bad shape as DCP_MLA_ERR_BAD_SHAPE)
+ * before the scratch limit is checked. The array is shared by every call on a
  * device and keeps the last call's contents (nothing in it has to start at
  * zero); calls whose work overlaps on the GPU — on different streams without
  * ordering between them — race on it and give undefined results.

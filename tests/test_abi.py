@@ -164,7 +164,8 @@ def test_fused_decode_rejects_bad_workspace_and_cp(lib):
     assert call(ws=FAKE + 128) == -106
     assert call(ws=None) == -106
     assert call(n_split=8) == -107          # 4 * 8 sources > 16
-    assert call(H=36) == -107               # 36 % 8 != 0
+    assert call(n_split=3) == -107          # 64 % 12 != 0
+    assert call(H=36) == -102               # not a multiple of 16: a shape error, reported first
     assert call(cp=0) == -107
 
 
@@ -219,3 +220,26 @@ def test_split_count_pick(lib):
         with pytest.raises(dcp.DcpError) as e:
             pick(*args)
         assert e.value.status == status
+
+
+def test_no_alloc_reports_bad_shapes_before_the_scratch_limit(lib):
+    # A shape the producer rejects is a shape error even when its partials
+    # would not fit the built-in scratch array; checked on the host, nothing
+    # launched, no device needed.
+    arr = ctypes.c_void_p * 8
+    ptrs = arr(*[FAKE] * 8)
+
+    def noalloc(B=64, H=128, Dk=576, Dv=512, T=100, cp=8, n_split=2):
+        return lib.dcp_mla_decode_noalloc(FAKE, ptrs, ptrs, cp, B, H, Dk, Dv, T, 0.1, 1, n_split, ptrs, None, None,
+                                          0, None)
+
+    def fused(B=64, H=128, Dk=576, Dv=512, T=100, cp=8, n_split=2, ws_bytes=1 << 20):
+        return lib.dcp_mla_decode(FAKE, ptrs, ptrs, cp, B, H, Dk, Dv, T, 0.1, 1, n_split, FAKE, ws_bytes, ptrs, None,
+                                  None, 0, None)
+
+    assert noalloc() == -108                      # valid shape, too large for the scratch
+    assert noalloc(Dv=4096) == -102 and noalloc(B=70000) == -102 and noalloc(Dk=640) == -102
+    assert noalloc(H=8, cp=1, n_split=1) == -102  # H not a multiple of 16
+    assert noalloc(n_split=17) == -103 and noalloc(cp=16) == -107
+    assert fused(Dv=4096) == -102 and fused(B=-1) == -102
+    assert fused() == -106                        # valid shape, workspace too small
