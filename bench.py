@@ -309,12 +309,15 @@ def time_graphs(graphs, reps: int, flush=None):
     return out
 
 
-def configs_extra(peak, flush):
-    """The other merge workloads, timed like the sweep (cold L2, PDL, 60
-    calls per graph, each on its own buffers where they fit): the DeepSeek-V2
-    sweep (cp=8, 128 heads, base-e [B, H, 1] LSE) and the speculative-decode
-    batch (1024 rows, 10% empty shards). For the latter the fraction of peak
-    uses the skip-aware bytes (empty shards' payloads are never read)."""
+def configs_extra(peak, flush, flags):
+    """The other merge workloads, timed like the sweep (cold L2, 60 calls per
+    graph, each on its own buffers where they fit, the sweep's launch flags):
+    the DeepSeek-V2 sweep (cp=8, 128 heads, base-e [B, H, 1] LSE) and the
+    speculative-decode batch (1024 rows, 10% empty shards). The default
+    schedule reads the empty shards' payloads too (it issues every payload
+    load beside the LSE loads), so its fraction of peak counts every byte; the
+    LSE_FIRST schedule, which never reads them, is timed beside it on the
+    skip-aware bytes."""
     import torch
     import decode_context_mla_dcp_gb300 as dcp
     from decode_context_mla_dcp_gb300.inputs import CONFIGS
@@ -328,18 +331,25 @@ def configs_extra(peak, flush):
             nbytes = dcp.algorithmic_bytes(cfg.cp, rows, cfg.H, cfg.D)
             slots = max(2, min(CALLS_PER_GRAPH, -(-4 * l2 // nbytes)))
             rs = RowSet(cfg, rows, slots)
-            g = rs.capture(dcp.DCP_FLAG_PDL)
+            g = rs.capture(flags)
             us = time_graphs({rows: g}, reps=10, flush=flush)[rows]
-            entry = {"us_per_call": round(us, 3), "bytes_per_call": nbytes,
-                     "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
-                     "frac_of_measured_peak": round(nbytes / (us * 1e-6) / 1e9 / peak, 4)}
+            gbs = nbytes / (us * 1e-6) / 1e9
+            entry = {"us_per_call": round(us, 3), "bytes_per_call": nbytes, "gbs": round(gbs, 1),
+                     "frac_of_measured_peak": round(gbs / peak, 4),
+                     "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
             if rs.inp.empty is not None:
-                skipped = int(rs.inp.empty.sum()) * cfg.H  # (row, head, source) payload rows never read
+                skipped = int(rs.inp.empty.sum()) * cfg.H  # (row, head, source) payload rows of weight 0
                 skip_bytes = dcp.algorithmic_bytes(cfg.cp, rows, cfg.H, cfg.D, skipped_payload_rows=skipped)
+                g2 = rs.capture(flags | dcp.DCP_FLAG_LSE_FIRST)
+                us2 = time_graphs({rows: g2}, reps=10, flush=flush)[rows]
+                del g2
                 entry["empty_row_shards"] = int(rs.inp.empty.sum())
-                entry["skip_aware_bytes_per_call"] = skip_bytes
-                entry["skip_aware_gbs"] = round(skip_bytes / (us * 1e-6) / 1e9, 1)
-                entry["frac_of_measured_peak"] = round(skip_bytes / (us * 1e-6) / 1e9 / peak, 4)
+                entry["schedule"] = "default (PRELOAD): reads every payload, zero-weight ones included"
+                entry["lse_first"] = {
+                    "us_per_call": round(us2, 3), "skip_aware_bytes_per_call": skip_bytes,
+                    "gbs": round(skip_bytes / (us2 * 1e-6) / 1e9, 1),
+                    "frac_of_measured_peak": round(skip_bytes / (us2 * 1e-6) / 1e9 / peak, 4),
+                    "schedule": "LSE_FIRST: reads the LSEs first and no zero-weight payload"}
             res[str(rows)] = entry
             del g, rs
             torch.cuda.empty_cache()
@@ -347,10 +357,12 @@ def configs_extra(peak, flush):
     return out
 
 
-def stress_extra(peak):
+def stress_extra(peak, flags, sample_rows: int = 32):
     """Bandwidth-stress config (cp=8, 128 heads, D=512, 4096 rows, base-e LSE
     U[0, 30]): 4.85 GB per call, cold by size. Inputs drawn on the device with
-    a seeded torch generator (same laws as the host generator; timing only)."""
+    a seeded torch generator (same laws as the host generator). The inputs and
+    outputs of `sample_rows` seeded rows of the timed call are kept on the host,
+    so the CPU-baseline leg can check those bytes against the oracle."""
     import torch
     import decode_context_mla_dcp_gb300 as dcp
     cp, H, D, B = 8, 128, 512, 4096
@@ -364,7 +376,7 @@ def stress_extra(peak):
     lout = [torch.empty((B, Hl), dtype=torch.float32, device="cuda") for _ in range(cp)]
 
     def call():
-        dcp.dcp_lse_reduce_ex(src, lse, cp, B, H, D, True, dcp.DCP_DTYPE_BF16, dst, lout, flags=dcp.DCP_FLAG_PDL)
+        dcp.dcp_lse_reduce_ex(src, lse, cp, B, H, D, True, dcp.DCP_DTYPE_BF16, dst, lout, flags=flags)
 
     for _ in range(3):
         call()
@@ -381,11 +393,36 @@ def stress_extra(peak):
     us = statistics.median(times)
     nbytes = dcp.algorithmic_bytes(cp, B, H, D)
     gbs = nbytes / (us * 1e-6) / 1e9
+    rows = np.sort(np.random.default_rng(2024).choice(B, size=sample_rows, replace=False))
+    idx = torch.from_numpy(rows).cuda()
+    sample = {"rows": rows.tolist(),
+              "srcs": [s[idx].contiguous().view(torch.int16).cpu().numpy().view(np.uint16) for s in src],
+              "lses": [l[idx].contiguous().cpu().numpy() for l in lse],
+              "outs": [d[idx].float().cpu().numpy().astype(np.float64) for d in dst],
+              "lse_outs": [l[idx].cpu().numpy().astype(np.float64) for l in lout]}
     del src, lse, dst, lout
     torch.cuda.empty_cache()
-    return {"workload": "bandwidth stress: cp=8, H=128, D=512, rows=4096, bf16, base-e LSE U[0,30]",
-            "us_per_call": round(us, 2), "bytes_per_call": nbytes, "gbs": round(gbs, 1),
-            "frac_of_measured_peak": round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
+    return ({"workload": "bandwidth stress: cp=8, H=128, D=512, rows=4096, bf16, base-e LSE U[0,30]",
+             "us_per_call": round(us, 2), "bytes_per_call": nbytes, "gbs": round(gbs, 1),
+             "frac_of_measured_peak": round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+             "parity_sample_rows": sample_rows}, sample)
+
+
+def stress_sample_parity(sample):
+    """The stress call's sampled rows (inputs and GPU outputs of the timed
+    launch) against the oracle, at the parity tests' tolerances."""
+    import oracle
+    ref, lref = oracle.merge(sample["srcs"], sample["lses"], True)
+    worst_out = worst_lse = 0.0
+    ok = True
+    for go, gl, ro, rl in zip(sample["outs"], sample["lse_outs"], ref, lref):
+        err = np.abs(go - ro)
+        ok &= bool((err <= 1e-2 + 8e-3 * np.abs(ro)).all()) and not bool(np.isnan(go).any())
+        worst_out = max(worst_out, float(err.max()))
+        lerr = np.abs(gl - rl) / np.maximum(np.abs(rl), 1.0)
+        ok &= bool((lerr <= 1e-5).all())
+        worst_lse = max(worst_lse, float(lerr.max()))
+    return {"ok": ok, "rows": len(sample["rows"]), "max_abs_err_out": worst_out, "max_rel_err_lse": worst_lse}
 
 
 def mla_extras(hbm_peak, tensor_peak):
@@ -453,10 +490,32 @@ def mla_extras(hbm_peak, tensor_peak):
         fl = [torch.empty((B, H // cp), dtype=torch.float32, device="cuda") for _ in range(cp)]
         us_f = timed(lambda k: dcp.mla_decode_dcp(q, shard_kvs[k], shard_lens, MLA_SCALE, n_split=n_split,
                                                   workspace=ws, outs=fo, lse_outs=fl, flags=dcp.DCP_FLAG_PDL))
+        # Its two launches apart. The producer's grid (cp*n_split slots of
+        # Ts/n_split tokens x head blocks x rows) is that of one producer call
+        # over the whole cache with cp*n_split splits, since shard j holds the
+        # cache's tokens [j*Ts, (j+1)*Ts). The merge alone reads the
+        # workspace's partials with the fused call's layout.
+        n_src = cp * n_split
+        pp = [torch.empty((B, H, 512), dtype=torch.bfloat16, device="cuda") for _ in range(n_src)]
+        ppl = [torch.empty((B, H), dtype=torch.float32, device="cuda") for _ in range(n_src)]
+        us_p = timed(lambda k: dcp.mla_decode_partial(q, kvs[k], lens, MLA_SCALE, n_split=n_src, outs=pp, lses=ppl,
+                                                      flags=dcp.DCP_FLAG_PDL))
+        Hs = H // n_src
+        m_dst = [fo[k // n_split].data_ptr() + (k % n_split) * Hs * 512 * 2 for k in range(n_src)]
+        m_lout = [fl[k // n_split].data_ptr() + (k % n_split) * Hs * 4 for k in range(n_src)]
+        lay = dcp.Layout(src_row=H * 512, src_head=512, lse_row=H, lse_head=1, dst_row=(H // cp) * 512,
+                         dst_head=512, lse_out_row=H // cp)
+        us_m = timed(lambda k: dcp.dcp_lse_reduce_ex(pp, ppl, n_src, B, H, 512, True, dcp.DCP_DTYPE_BF16, m_dst,
+                                                     m_lout, layout=lay, flags=dcp.DCP_FLAG_PDL))
         out[f"fused producer+merge, {name}"] = {
             "shape": f"B={B}, H={H}, cp={cp} shards x {Ts} tokens, n_split={n_split}", "us_per_call": round(us_f, 2),
-            "kv_gbs": round(kv_bytes / us_f / 1e3, 1), "tflops": round(flops / us_f / 1e6, 1)}
-        del q, kvs, shard_kvs, po, pl, ws, fo, fl
+            "kv_gbs": round(kv_bytes / us_f / 1e3, 1), "tflops": round(flops / us_f / 1e6, 1),
+            "producer_alone_us": round(us_p, 2), "merge_alone_us": round(us_m, 2),
+            "fused_minus_parts_us": round(us_f - us_p - us_m, 2),
+            "how_split": "producer alone = one producer call over the whole cache with cp*n_split splits (the fused "
+                         "launch's grid); merge alone = the merge over those partials with the fused layout; each "
+                         "timed like the fused call (ten calls per graph, PDL)"}
+        del q, kvs, shard_kvs, po, pl, ws, fo, fl, pp, ppl
         torch.cuda.empty_cache()
     return out
 
@@ -580,7 +639,7 @@ def cpu_baseline(cfg, budget_s: float = 12.0):
 
 
 def sweep_parity(cfg, inputs):
-    """The timed path (dcp_lse_reduce_ex with PDL) on the sweep's inputs
+    """The timed path (dcp_lse_reduce_ex with the sweep's flags) on its inputs
     against the oracle: outputs within |gpu - ref| <= 1e-2 + 8e-3 |ref|,
     merged LSEs within 1e-5 * max(|ref|, 1)."""
     import torch
@@ -591,7 +650,7 @@ def sweep_parity(cfg, inputs):
     for inp in inputs:
         srcs = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda() for x in inp.srcs]
         lses = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in inp.lses]
-        got_o, got_l = dcp.merge(srcs, lses, inp.lse_base_e, flags=dcp.DCP_FLAG_PDL)
+        got_o, got_l = dcp.merge(srcs, lses, inp.lse_base_e, flags=dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH)
         torch.cuda.synchronize()
         ref_o, ref_l = oracle.merge(inp.srcs, inp.lses, inp.lse_base_e)
         for go, gl, ro, rl in zip(got_o, got_l, ref_o, ref_l):
@@ -689,6 +748,8 @@ def config_dict(cfg):
                         f"D={cfg.D}, bf16 partials N(0,1), base-2 fp32 LSE U[-4,24], rows {list(cfg.rows)}",
             "cp": cfg.cp, "heads": cfg.H, "head_dim": cfg.D, "rows": list(cfg.rows),
             "calls_per_graph": CALLS_PER_GRAPH,
+            "launch": "programmatic dependent launch; each warp brings its inputs into L2 before it waits for the "
+                      "previous call (DCP_FLAG_PDL | DCP_FLAG_PREFETCH)",
             "l2": "flushed before every step (write of 4x L2); each of a graph's 60 calls has its own buffers",
             "parallelism": "replicas (one independent merge workload per GPU)"}
 
@@ -717,7 +778,7 @@ def run_ours(args):
     except Exception:
         pass
 
-    flags = dcp.DCP_FLAG_PDL
+    flags = dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH
     bytes_per_rows = sweep_bytes(cfg)
     step_bytes = sum(bytes_per_rows.values()) * CALLS_PER_GRAPH
     sets = {rows: RowSet(cfg, rows, CALLS_PER_GRAPH) for rows in cfg.rows}
@@ -786,22 +847,28 @@ def run_ours(args):
     if rank == 0 and not args.no_extras:
         hot = {rows: sets[rows].capture(flags, same_slot=True) for rows in cfg.rows}
         nopdl = {rows: sets[rows].capture(0) for rows in cfg.rows}
+        nopf = {rows: sets[rows].capture(dcp.DCP_FLAG_PDL) for rows in cfg.rows}
         hot_us = time_graphs(hot, 20)
         cold_nopdl_us = time_graphs(nopdl, 20, flush=flush)
+        cold_nopf_us = time_graphs(nopf, 20, flush=flush)
         out["extras"] = {
             "l2_hot_us_per_call": {str(r): round(v, 3) for r, v in hot_us.items()},
-            "cold_no_pdl_us_per_call": {str(r): round(v, 3) for r, v in cold_nopdl_us.items()},
+            "cold_no_pdl_no_prefetch_us_per_call": {str(r): round(v, 3) for r, v in cold_nopdl_us.items()},
+            "cold_pdl_no_prefetch_us_per_call": {str(r): round(v, 3) for r, v in cold_nopf_us.items()},
         }
-        del hot, nopdl
+        del hot, nopdl, nopf
     out["e2e"] = e2e_measure(cfg, max(10, min(args.steps, 100)))
+    stress_sample = None
     if rank == 0 and not args.no_extras:
         del sets, graphs
         torch.cuda.empty_cache()
-        out["extras"]["other_configs_cold_pdl"] = configs_extra(peak, flush)
-        out["extras"]["largest_config"] = stress_extra(peak)
+        out["extras"]["other_configs_cold"] = configs_extra(peak, flush, flags)
+        out["extras"]["largest_config"], stress_sample = stress_extra(peak, flags)
         out["extras"]["dcp_producer_and_fused_decode"] = mla_extras(peak, measured_tensor_peak())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg)
+        if stress_sample is not None:
+            out["cpu_baseline"]["parity_vs_oracle"]["stress_sample"] = stress_sample_parity(stress_sample)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -835,7 +902,7 @@ def run_case(args):
         return 0
     cfg = CONFIGS[args.case]
     rows_list = [int(r) for r in args.rows.split(",")] if args.rows else list(cfg.rows)
-    flags = dcp.DCP_FLAG_PDL
+    flags = dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH
     for rows in rows_list:
         inp = make_merge_inputs(cfg, rows, seed=0)
         Hl = cfg.H // cfg.cp
