@@ -38,6 +38,7 @@ constexpr int kDv = 512;
 constexpr int kNt = 32;              // tokens per KV tile
 constexpr int kSPad = 4;             // fp32 padding of a score row in shared memory
 constexpr unsigned kFlagPdl = 1u;
+constexpr unsigned kFlagPrefetch = 8u;  // DCP_FLAG_PREFETCH: L2 prefetch of the first tile before the PDL wait
 constexpr unsigned kFlagMmaSync = 2u;   // DCP_MLA_FLAG_MMA_SYNC
 constexpr unsigned kFlagTcgen05 = 4u;   // DCP_MLA_FLAG_TCGEN05
 // When the tcgen05 kernel is the default. Its MMAs cost about the same per
@@ -72,7 +73,7 @@ __host__ __device__ constexpr int row_bytes() {
 template <int kDk, int kG>
 __host__ __device__ constexpr int smem_bytes() {
     return 16 * kG * row_bytes<kDk>() + 2 * kNt * row_bytes<kDk>() + 16 * kG * (kNt + kSPad) * 4 + kG * 2 * 256 * 4 +
-           3 * 8;
+           3 * 8 + 16;
 }
 
 // ---- PTX helpers -------------------------------------------------------------
@@ -104,18 +105,34 @@ __device__ __forceinline__ long long global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Wait for a phase of an mbarrier, giving up after kWaitLimitNs: then the
-// status word records it and the caller carries on (the outputs are invalid,
-// but the kernel ends).
-__device__ __forceinline__ void mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
-    if (mbar_try_wait(bar, parity)) return;
+// The waits of both kernels. Every thread of a CTA shares one abort
+// flag in shared memory: a wait that has not seen its phase after
+// kWaitLimitNs sets it (and ORs 1 into the status word), and from then on
+// every wait of the CTA returns at once. Returns whether the phase completed.
+// The kernel stops issuing copies and MMAs, leaves its tile loop at the next
+// tile boundary (a barrier vote, so all threads leave together), skips the
+// epilogue (the outputs are not valid) and drains the copies and MMAs it
+// armed before it frees TMEM and exits.
+__device__ __forceinline__ bool mbar_wait_cta(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
         if (global_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
             if (status != nullptr) atomicOr(status, 1);
-            return;
+            return false;
         }
     }
+    return true;
+}
+// Bounded wait that ignores the abort flag: the drain before TMEM is freed.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
 }
 // One contiguous global -> shared copy by the bulk-copy engine.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -169,6 +186,8 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
     float* const s_s = reinterpret_cast<float*>(kv_s + 2 * kNt * kRow);   // [kHB][kSRow] scores of a tile
     float* const s_part = s_s + kHB * kSRow;                              // [kG][2][16][16] half-Dk partial scores
     uint64_t* const bars = reinterpret_cast<uint64_t*>(s_part + kG * 2 * 256);  // [0] Q, [1], [2] KV buffers
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(bars + 3);  // see mbar_wait_cta
+    int* const armed = reinterpret_cast<int*>(bars + 3) + 1;                      // [2]: last tile loaded per buffer
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = warp % kG;    // head group: heads [16g, 16g+16) of the block
@@ -190,6 +209,8 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         mbar_init(&bars[2], 1);
+        *abort_flag = 0;
+        armed[0] = armed[1] = -1;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -226,6 +247,7 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
         mbar_expect_tx(&bars[1 + buf], (uint32_t)(rows * kDk * 2));
         for (int r = 0; r < rows; ++r)
             bulk_g2s(dst + r * kRow, kv_row + ((int64_t)i * kNt + r) * kDk * 2, kDk * 2, &bars[1 + buf]);
+        armed[buf] = i;
     };
     if (threadIdx.x == 0) {
         mbar_expect_tx(&bars[0], (uint32_t)(kHB * kDk * 2));
@@ -234,7 +256,7 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
         load_tile(0, 0);
         if (ntiles > 1) load_tile(1, 1);
     }
-    mbar_wait(&bars[0], 0, p.status);
+    (void)mbar_wait_cta(&bars[0], 0, abort_flag, p.status);
 
     // per-lane state: rows gr and gr+8 of the warp's 16 heads
     float m_run[2] = {-INFINITY, -INFINITY};  // running max, base-2 units
@@ -250,9 +272,10 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
     const uint32_t v_off = ((lane & 7) + (((lane >> 3) & 1) << 3)) * kRow + (128 * q4 + (lane >> 4) * 8) * 2;
     float* const part = s_part + (g * 2 + th) * 256;  // 16 x 16 partial of (group, token half)
 
+    bool aborted = false;  // CTA-uniform: decided by a barrier vote at the end of each tile
     for (int i = 0; i < ntiles; ++i) {
         const int buf = i & 1;
-        mbar_wait(&bars[1 + buf], (uint32_t)((i >> 1) & 1), p.status);
+        (void)mbar_wait_cta(&bars[1 + buf], (uint32_t)((i >> 1) & 1), abort_flag, p.status);
         const uint32_t kt = smem_u32(kv_s + buf * kNt * kRow);
 
         // partial scores: 16 heads x 16 tokens over half of Dk
@@ -355,11 +378,24 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
                 mma_bf16(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
             }
         }
-        __syncthreads();  // every warp is done with this KV buffer and the score tile
+        // every warp is done with this KV buffer and the score tile; all threads
+        // stop together once any wait gave up
+        if (__syncthreads_or(*abort_flag != 0)) {
+            aborted = true;
+            break;
+        }
         if (threadIdx.x == 0 && i + 2 < ntiles) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             load_tile(i + 2, buf);
         }
+    }
+    if (aborted) {  // outputs not valid (status says so); no copy may still land in shared memory
+        if (threadIdx.x == 0) {
+            (void)mbar_wait_drain(&bars[0], 0);
+            for (int k = 0; k < 2; ++k)
+                if (armed[k] >= 0) (void)mbar_wait_drain(&bars[1 + k], (uint32_t)((armed[k] >> 1) & 1));
+        }
+        return;
     }
 
     // normalise, round to bf16, store; LSE = m + log2(l), in the requested base
@@ -414,6 +450,7 @@ struct TcParams {
     int H, n_split;
     float scale_log2;
     float lse_scale;
+    int prefetch;                     // 1: bring Q and the first KV tile into L2 before the PDL wait
 };
 
 template <int kDk, int kNH>
@@ -549,14 +586,18 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
     uint8_t* const p_s = kPInRope ? kv_s + 8 * kTcAtom : q_s + kAtoms * kQAtom;
     uint8_t* const misc = kPInRope ? q_s + kAtoms * kQAtom : p_s + 2 * kQAtom;
     uint64_t* const bar_q = reinterpret_cast<uint64_t*>(misc);
-    uint64_t* const bar_kv = bar_q + 1;
-    uint64_t* const bar_s = bar_q + 2;
-    uint64_t* const bar_o = bar_q + 3;
-    uint32_t* const tslot = reinterpret_cast<uint32_t*>(bar_q + 4);
-    float* const red = reinterpret_cast<float*>(misc + 64);  // [4][kNH]
+    uint64_t* const bar_kv = bar_q + 1;                      // a KV tile has landed
+    uint64_t* const bar_s = bar_q + 2;                       // score MMAs of a tile done
+    uint64_t* const bar_o = bar_q + 3;                       // value MMAs of a tile done
+    uint32_t* const tslot = reinterpret_cast<uint32_t*>(misc + 32);
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 36);
+    int* const armed = reinterpret_cast<int*>(misc + 40);   // [4]: last tile each barrier was armed for
+    float* const red = reinterpret_cast<float*>(misc + 128); // [4][kNH]
     float* const m_s = red + 4 * kNH;                        // running max per head (base-2 units)
     float* const a_s = m_s + kNH;                            // this tile's rescale factor per head
     float* const t_s = a_s + kNH;                            // tile max, then the final sums
+    static_assert(128 + 7 * kNH * 4 <= kTcMiscBytes, "misc area");
+    constexpr int kArmQ = 0, kArmKv = 1, kArmS = 2, kArmO = 3;  // indices into armed[]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int slot = blockIdx.x;
@@ -575,6 +616,8 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_q)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_kv[shard])) : "memory");
     }
+    if (tid < 4) armed[tid] = -1;
+    if (tid == 4) *abort_flag = 0;
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
                      "r"(kCols)
@@ -591,6 +634,23 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
     const int quad = warp & 3, tok = tid & 127, hb = (warp >> 2) * kHW;
     const uint32_t tlane = (uint32_t)(32 * quad) << 16;
 
+    // With DCP_FLAG_PREFETCH, Q and the split's first KV tile are brought into
+    // L2 before the wait (a hint, so the loads after the wait still see what the
+    // previous kernel wrote). The split's start needs kv_len, an input: the
+    // prefetch takes the value before the wait, and a stale one only prefetches
+    // other rows.
+    if (p.prefetch && tid == 32) {
+        int64_t len0 = p.kv_len[shard][b];
+        len0 = len0 < 0 ? 0 : (len0 > p.T ? p.T : len0);
+        const int64_t t0 = (int64_t)split * ((len0 + p.n_split - 1) / p.n_split);
+        if (t0 < len0) {
+            for (int a = 0; a < kAtoms; ++a) {
+                tma_prefetch_2d(&p.tm_q, a * 64, b * p.H + h0);
+                tma_prefetch_2d(&p.tm_kv[shard], a * 64, (int)((int64_t)b * p.T + t0));
+            }
+        }
+    }
+
     pdl_wait();
     pdl_launch_dependents();
 
@@ -603,6 +663,7 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
     uint8_t* const out = p.out[slot];
     float* const lse = p.lse[slot];
     const int64_t out_row0 = ((int64_t)b * p.H + h0) * kDv;
+    bool aborted = false;  // CTA-uniform: decided by barrier votes
 
     if (ntok == 0) {  // empty range: output 0, LSE -inf
         for (int i = tid; i < kNH * kDv / 8; i += (int)blockDim.x)
@@ -614,24 +675,31 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
         if (tid == 0) {
             mbar_expect_tx(bar_q, (uint32_t)(kAtoms * kQAtom));
             for (int a = 0; a < kAtoms; ++a) tma_load_2d(q_s + a * kQAtom, &p.tm_q, a * 64, b * p.H + h0, bar_q);
+            armed[kArmQ] = 0;
             mbar_expect_tx(bar_kv, (uint32_t)(kAtoms * kTcAtom));
             for (int a = 0; a < kAtoms; ++a) tma_load_2d(kv_s + a * kTcAtom, &p.tm_kv[shard], a * 64, row0, bar_kv);
+            armed[kArmKv] = 0;
         }
         float l_part[kHW];  // this thread's token's share of each of its heads' sums
 #pragma unroll
         for (int h = 0; h < kHW; ++h) l_part[h] = 0.f;
-        mbar_wait(bar_q, 0, p.status);
+        (void)mbar_wait_cta(bar_q, 0, abort_flag, p.status);
 
         for (int i = 0; i < ntiles; ++i) {
+            // Stop at a tile boundary, all threads together, once any wait gave up.
+            if (__syncthreads_or(*abort_flag != 0)) {
+                aborted = true;
+                break;
+            }
             const uint32_t ph = (uint32_t)(i & 1);
-            mbar_wait(bar_kv, ph, p.status);
+            (void)mbar_wait_cta(bar_kv, ph, abort_flag, p.status);
             // Start the next tile's DRAM reads now, into L2 (from a thread of another
             // warp than the MMA issuer's), so that its load after this tile's value
             // MMAs streams from L2: every CTA reloads at about the same moment, and
             // from DRAM those loads contend.
             if (tid == 32 && i + 1 < ntiles)
                 for (int a = 0; a < kAtoms; ++a) tma_prefetch_2d(&p.tm_kv[shard], a * 64, row0 + (i + 1) * kTcTok);
-            if (tid == 0) {  // scores: S^T = K_tile . Q^T
+            if (tid == 0 && !*abort_flag) {  // scores: S^T = K_tile . Q^T
                 tc_fence_after();
 #pragma unroll 1
                 for (int a = 0; a < kAtoms; ++a) {
@@ -643,8 +711,9 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
                     }
                 }
                 umma_commit(bar_s);
+                armed[kArmS] = i;
             }
-            mbar_wait(bar_s, ph, p.status);
+            (void)mbar_wait_cta(bar_s, ph, abort_flag, p.status);
             tc_fence_after();
 
             float sv[kHW];
@@ -655,13 +724,18 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
             const bool live = tok < valid;
 #pragma unroll
             for (int h = 0; h < kHW; ++h) sv[h] = live ? sv[h] * p.scale_log2 : -INFINITY;
-            if (!live) {  // a token past the range: its value row must be finite (0 x V)
+            // A token past the range gets probability 0. Inside the row's first len
+            // cache rows it is another split's token, finite, and adds 0 x V = 0; a
+            // row at or past len may hold anything (NaN), so its value row is zeroed.
+            // (Chunk order rotated by token: the rows of a warp's tokens lie 128 bytes
+            // apart, on the same banks.)
+            if (t_begin + (int64_t)i * kTcTok + tok >= len) {
                 constexpr int kPerGroup = 8 / tc_head_groups<kNH>();  // latent slices zeroed per thread
 #pragma unroll 1
                 for (int a = (warp >> 2) * kPerGroup; a < (warp >> 2) * kPerGroup + kPerGroup; ++a) {
                     uint4* row = reinterpret_cast<uint4*>(kv_s + a * kTcAtom + (tok >> 3) * 1024 + (tok & 7) * 128);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+                    for (int c = 0; c < 8; ++c) row[(c + tok) & 7] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             // The running max moves only when some head's tile max exceeds it by more
@@ -688,7 +762,7 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
                 __syncthreads();
             }
             if (any && i > 0) {  // rescale O^T (the previous tile's value MMAs are done)
-                mbar_wait(bar_o, (uint32_t)((i - 1) & 1), p.status);
+                (void)mbar_wait_cta(bar_o, (uint32_t)((i - 1) & 1), abort_flag, p.status);
                 tc_fence_after();
 #pragma unroll 1
                 for (int m = 0; m < 4; ++m) {
@@ -728,16 +802,26 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
 #pragma unroll
                     for (int h = 0; h < kHW; ++h) l_part[h] += sv[h];
                 }
+                // P^T row h holds head h over the tile's tokens. Neighbouring lanes hold
+                // neighbouring tokens: they swap one value per pair of heads, so each
+                // lane converts and stores two tokens of one head in one 4-byte word
+                // (the even lane head h, the odd lane head h + 1).
                 uint8_t* const prow = p_s + (tok >> 6) * kQAtom;
-                const int tl = tok & 63;
+                const int tl = tok & 62;  // the pair's first token
+                const bool odd = (lane & 1) != 0;
 #pragma unroll
-                for (int h = 0; h < kHW; ++h)
-                    *reinterpret_cast<__nv_bfloat16*>(prow + sw128(hb + h, tl)) = __float2bfloat16_rn(sv[h]);
+                for (int h = 0; h < kHW; h += 2) {
+                    const float give = odd ? sv[h] : sv[h + 1];
+                    const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+                    const int hh = hb + h + (odd ? 1 : 0);
+                    const __nv_bfloat162 v = odd ? __floats2bfloat162_rn(got, sv[h + 1]) : __floats2bfloat162_rn(sv[h], got);
+                    *reinterpret_cast<__nv_bfloat162*>(prow + sw128(hh, tl)) = v;
+                }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             __syncthreads();
-            if (tid == 0) {  // values: O^T += V_tile^T . P^T, four 128-row blocks of the 512 latent dims
+            if (tid == 0 && !*abort_flag) {  // values: O^T += V_tile^T . P^T, four 128-row blocks of the 512 latent dims
                 tc_fence_after();
 #pragma unroll 1
                 for (int m = 0; m < 4; ++m) {
@@ -749,45 +833,81 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
                     }
                 }
                 umma_commit(bar_o);
-                if (i + 1 < ntiles) {  // the next tile reuses every buffer once these MMAs are done
-                    mbar_wait(bar_o, ph, p.status);
+                armed[kArmO] = i;
+                // the next tile reuses every buffer once these MMAs are done
+                if (i + 1 < ntiles && mbar_wait_cta(bar_o, ph, abort_flag, p.status)) {
                     mbar_expect_tx(bar_kv, (uint32_t)(kAtoms * kTcAtom));
                     for (int a = 0; a < kAtoms; ++a)
                         tma_load_2d(kv_s + a * kTcAtom, &p.tm_kv[shard], a * 64, row0 + (i + 1) * kTcTok, bar_kv);
+                    armed[kArmKv] = i + 1;
                 }
             }
         }
 
-        // final sums, then normalise, round to bf16 and store; LSE = m + log2(l)
-        mbar_wait(bar_o, (uint32_t)((ntiles - 1) & 1), p.status);
-        tc_fence_after();
-        cta_reduce_heads<kNH, kHW, true>(l_part, quad, hb, lane, red, t_s);
-        // The [kNH, 512] output tile is assembled in the KV buffer (free now:
-        // every MMA is done and no load is pending), then leaves in one bulk
-        // copy: rows h0 .. h0+kNH-1 of out[b] are contiguous.
-        __nv_bfloat16* const o_s = reinterpret_cast<__nv_bfloat16*>(kv_s);
-#pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
-#pragma unroll
-            for (int c = hb; c < hb + kHW; c += 16) {
-                float ov[16];
-                tmem_ld16(tmem + tlane + kNH + m * kNH + c, ov);
-                tmem_wait_ld();
-                const int dv = 128 * m + 32 * quad + lane;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) o_s[(c + j) * kDv + dv] = __float2bfloat16_rn(ov[j] / t_s[c + j]);
-            }
+        if (!aborted) {
+            // final sums, then normalise, round to bf16 and store; LSE = m + log2(l)
+            (void)mbar_wait_cta(bar_o, (uint32_t)((ntiles - 1) & 1), abort_flag, p.status);
+            aborted = __syncthreads_or(*abort_flag != 0) != 0;
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (!aborted) {
+            tc_fence_after();
+            cta_reduce_heads<kNH, kHW, true>(l_part, quad, hb, lane, red, t_s);
+            if (tid < kNH) a_s[tid] = 1.0f / t_s[tid];  // one reciprocal per head, then products
+            __syncthreads();
+            // The [kNH, 512] output tile is assembled in the KV buffer (free now:
+            // every MMA is done and no load is pending), then leaves in one bulk
+            // copy: rows h0 .. h0+kNH-1 of out[b] are contiguous.
+            __nv_bfloat16* const o_s = reinterpret_cast<__nv_bfloat16*>(kv_s);
+            // This thread's latent dim of each 128-row block, all its heads: every
+            // TMEM load issued before one wait.
+            float ov[4][kHW];
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int c = 0; c < kHW; c += 16) tmem_ld16(tmem + tlane + kNH + m * kNH + hb + c, ov[m] + c);
+            tmem_wait_ld();
+            // lane = latent dim: neighbouring lanes swap one value per pair of heads,
+            // so each lane converts and stores two dims of one head in one word
+            const bool odd = (lane & 1) != 0;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int dv = 128 * m + 32 * quad + (lane & ~1);  // the pair's first dim
+#pragma unroll
+                for (int j = 0; j < kHW; j += 2) {
+                    const float x0 = ov[m][j] * a_s[hb + j], x1 = ov[m][j + 1] * a_s[hb + j + 1];
+                    const float got = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
+                    const int hh = hb + j + (odd ? 1 : 0);
+                    *reinterpret_cast<__nv_bfloat162*>(o_s + hh * kDv + dv) =
+                        odd ? __floats2bfloat162_rn(got, x1) : __floats2bfloat162_rn(x0, got);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncthreads();
+            if (tid == 0) {
+                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(out + out_row0 * 2),
+                             "r"(smem_u32(o_s)), "r"((uint32_t)(kNH * kDv * 2))
+                             : "memory");
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
+            if (tid < kNH) lse[(int64_t)b * p.H + h0 + tid] = (m_s[tid] + log2f(t_s[tid])) * p.lse_scale;
+            // before the CTA leaves, the copy must have read the tile out of shared
+            // memory (its global writes are visible to later kernels once this grid
+            // completes)
+            if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        }
+    }
+    if (aborted) {
+        // A wait gave up (the status word says so; the outputs are not valid).
+        // Before TMEM is freed and the CTA leaves, wait (bounded) for every copy
+        // and MMA this CTA armed, so none still writes into its shared memory or
+        // TMEM.
         __syncthreads();
         if (tid == 0) {
-            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(out + out_row0 * 2),
-                         "r"(smem_u32(o_s)), "r"((uint32_t)(kNH * kDv * 2))
-                         : "memory");
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            if (armed[kArmQ] >= 0) (void)mbar_wait_drain(bar_q, 0);
+            if (armed[kArmKv] >= 0) (void)mbar_wait_drain(bar_kv, (uint32_t)(armed[kArmKv] & 1));
+            if (armed[kArmS] >= 0) (void)mbar_wait_drain(bar_s, (uint32_t)(armed[kArmS] & 1));
+            if (armed[kArmO] >= 0) (void)mbar_wait_drain(bar_o, (uint32_t)(armed[kArmO] & 1));
         }
-        if (tid < kNH) lse[(int64_t)b * p.H + h0 + tid] = (m_s[tid] + log2f(t_s[tid])) * p.lse_scale;
-        if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the copy has landed
     }
     tc_fence_before();
     __syncthreads();
@@ -919,7 +1039,7 @@ bool tc_is_default(int H, int64_t tokens_per_split) {
 extern "C" int dcp_mla_decode_kernel(int H, int64_t T, int n_split, unsigned flags) {
     if (H < 16 || H % 16 != 0 || T < 0) return DCP_MLA_ERR_BAD_SHAPE;
     if (n_split < 1 || n_split > DCP_MLA_SPLIT_MAX) return DCP_MLA_ERR_BAD_SPLIT;
-    if ((flags & ~(kFlagPdl | kFlagMmaSync | kFlagTcgen05)) != 0) return DCP_MLA_ERR_BAD_FLAGS;
+    if ((flags & ~(kFlagPdl | kFlagPrefetch | kFlagMmaSync | kFlagTcgen05)) != 0) return DCP_MLA_ERR_BAD_FLAGS;
     if ((flags & kFlagMmaSync) && (flags & kFlagTcgen05)) return DCP_MLA_ERR_BAD_FLAGS;
     if (flags & kFlagTcgen05) return DCP_MLA_KERNEL_TCGEN05;
     if (flags & kFlagMmaSync) return DCP_MLA_KERNEL_MMA_SYNC;
@@ -968,7 +1088,7 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
     if (!shape_ok(B, H, Dk, Dv, T)) return DCP_MLA_ERR_BAD_SHAPE;
     if (n_split < 1 || n_split > DCP_MLA_SPLIT_MAX) return DCP_MLA_ERR_BAD_SPLIT;
     if (n_shard < 1 || n_shard * n_split > kSlots) return DCP_MLA_ERR_BAD_CP;
-    if ((flags & ~(kFlagPdl | kFlagMmaSync | kFlagTcgen05)) != 0) return DCP_MLA_ERR_BAD_FLAGS;
+    if ((flags & ~(kFlagPdl | kFlagPrefetch | kFlagMmaSync | kFlagTcgen05)) != 0) return DCP_MLA_ERR_BAD_FLAGS;
     if ((flags & kFlagMmaSync) && (flags & kFlagTcgen05)) return DCP_MLA_ERR_BAD_FLAGS;
     if (!aligned(q, 16) || (status != nullptr && !aligned(status, 4))) return DCP_MLA_ERR_MISALIGNED;
     Params prm;
@@ -1016,6 +1136,7 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
         tp.n_split = n_split;
         tp.scale_log2 = scale * 1.4426950408889634f;
         tp.lse_scale = lse_base_e ? 0.6931471805599453f : 1.0f;
+        tp.prefetch = (flags & kFlagPrefetch) ? 1 : 0;
         const cudaError_t e = Dk == 576 ? launch_tc_dk<576>(tp, B, n_slots, flags & kFlagPdl, st)
                                         : launch_tc_dk<512>(tp, B, n_slots, flags & kFlagPdl, st);
         if (e != cudaSuccess) {

@@ -43,8 +43,11 @@
  *            16-byte aligned
  *   lse_ptrs host array of n_split device pointers, each [B, H] fp32
  *   status   NULL, or a device int32 the kernel ORs 1 into if a wait for its
- *            own asynchronous copies ever exceeds two seconds (then the
- *            outputs are not valid); it never hangs.
+ *            own asynchronous copies or MMAs ever exceeds two seconds. Then
+ *            the CTA stops issuing copies and MMAs, leaves at the next tile
+ *            boundary without writing its outputs (they are not valid), waits
+ *            (again at most two seconds each) for what it had issued, frees
+ *            its tensor memory and exits: it never hangs.
  *
  * Asynchrony, ownership, errors: as for dcp_lse_reduce (one kernel enqueued
  * on `stream`, nothing allocated, graph-capturable; negative codes are host
@@ -68,7 +71,8 @@ enum {
     DCP_MLA_ERR_BAD_SPLIT = -103,    /* n_split outside [1, DCP_MLA_SPLIT_MAX] */
     DCP_MLA_ERR_MISALIGNED = -104,   /* q, kv or an output not 16-byte aligned, or an LSE or kv_len
                                         pointer not 4-byte aligned */
-    DCP_MLA_ERR_BAD_FLAGS = -105,    /* unknown flag bits, or both DCP_MLA_FLAG_MMA_SYNC and DCP_MLA_FLAG_TCGEN05 */
+    DCP_MLA_ERR_BAD_FLAGS = -105,    /* unknown flag bits (DCP_FLAG_PDL, DCP_FLAG_PREFETCH and the two below
+                                        are known), or both DCP_MLA_FLAG_MMA_SYNC and DCP_MLA_FLAG_TCGEN05 */
     DCP_MLA_ERR_WORKSPACE = -106,    /* workspace NULL, not 256-byte aligned, or smaller than
                                         dcp_mla_decode_workspace_bytes(...) */
     DCP_MLA_ERR_BAD_CP = -107,       /* cp < 1, cp*n_split > 16, or H not a multiple of cp*n_split */
@@ -89,6 +93,14 @@ enum {
  */
 #define DCP_MLA_FLAG_MMA_SYNC 2u
 #define DCP_MLA_FLAG_TCGEN05 4u
+/*
+ * DCP_FLAG_PREFETCH (8, include/dcp_lse_reduce.h) is also taken by the
+ * producer: each CTA of the tcgen05 kernel brings Q and its split's first KV
+ * tile into L2 before it waits for the previous kernel (with DCP_FLAG_PDL that
+ * wait overlaps the previous kernel's tail). A hint: results are the same.
+ * dcp_mla_decode passes it to the producer only, not to its merge (whose
+ * inputs the producer has just written).
+ */
 
 int dcp_mla_decode_partial(const void* q, const void* kv, const int32_t* kv_len,
                            int64_t B, int H, int Dk, int Dv, int64_t T, float scale, int lse_base_e,

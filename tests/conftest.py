@@ -23,3 +23,20 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+# Worst errors the GPU tests observed, by quantity (printed at the end of the
+# run): the tolerances' margins, as measured.
+WORST_ERRORS: dict = {}
+
+
+def record_error(what: str, value: float) -> None:
+    if value > WORST_ERRORS.get(what, -1.0):
+        WORST_ERRORS[what] = float(value)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    if WORST_ERRORS:
+        terminalreporter.write_sep("-", "worst observed errors")
+        for k in sorted(WORST_ERRORS):
+            terminalreporter.write_line(f"{k}: {WORST_ERRORS[k]:.3e}")

@@ -130,7 +130,8 @@ def test_mla_producer_rejects_bad_arguments(lib):
     assert call(Dk=640) == -102 and call(Dv=256) == -102 and call(T=-1) == -102
     assert call(n_split=0) == -103 and call(n_split=17) == -103
     assert call(q=FAKE + 8) == -104 and call(kv_len=FAKE + 2) == -104 and call(o=arr(FAKE + 4, FAKE)) == -104
-    assert call(flags=8) == -105 and call(flags=6) == -105
+    assert call(flags=16) == -105 and call(flags=6) == -105
+    assert call(flags=dcp.DCP_FLAG_PREFETCH | dcp.DCP_FLAG_PDL, B=0) == 0  # the producer takes the prefetch flag
     assert call(B=0) == 0  # nothing to do, nothing launched
     assert dcp.dcp_mla_decode_smem_bytes(576, 64) > 150000
     assert "n_split" in dcp.dcp_lse_reduce_strerror(-103)
@@ -183,9 +184,9 @@ def test_producer_kernel_choice(lib):
     assert k(16, 1 << 20, 1) == mma and k(48, 1 << 20, 1) == mma
     # forcing flags (PDL does not change the choice)
     assert k(16, 64, 1, dcp.DCP_MLA_FLAG_TCGEN05) == tc and k(128, 1 << 20, 1, dcp.DCP_MLA_FLAG_MMA_SYNC) == mma
-    assert k(128, 4096, 1, dcp.DCP_FLAG_PDL) == tc
+    assert k(128, 4096, 1, dcp.DCP_FLAG_PDL) == tc and k(128, 4096, 1, dcp.DCP_FLAG_PREFETCH) == tc
     for args, status in [((128, 4096, 1, dcp.DCP_MLA_FLAG_TCGEN05 | dcp.DCP_MLA_FLAG_MMA_SYNC), -105),
-                         ((128, 4096, 1, 8), -105), ((128, 4096, 0), -103), ((128, 4096, 17), -103),
+                         ((128, 4096, 1, 16), -105), ((128, 4096, 0), -103), ((128, 4096, 17), -103),
                          ((20, 4096, 1), -102), ((128, -1, 1), -102)]:
         with pytest.raises(dcp.DcpError) as e:
             k(*args)
