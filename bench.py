@@ -466,10 +466,13 @@ def mla_extras(hbm_peak, tensor_peak):
                 ts.append(a.elapsed_time(e) * 1e3 / n_calls)
             return statistics.median(ts)
 
+        pf = dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH
         us = timed(lambda k: dcp.mla_decode_partial(q, kvs[k], lens, MLA_SCALE, n_split=ns, outs=po, lses=pl,
-                                                    flags=dcp.DCP_FLAG_PDL))
+                                                    flags=pf))
+        us_nopf = timed(lambda k: dcp.mla_decode_partial(q, kvs[k], lens, MLA_SCALE, n_split=ns, outs=po, lses=pl,
+                                                         flags=dcp.DCP_FLAG_PDL))
         us_mma = timed(lambda k: dcp.mla_decode_partial(q, kvs[k], lens, MLA_SCALE, n_split=ns, outs=po, lses=pl,
-                                                        flags=dcp.DCP_FLAG_PDL | dcp.DCP_MLA_FLAG_MMA_SYNC))
+                                                        flags=pf | dcp.DCP_MLA_FLAG_MMA_SYNC))
         kv_bytes = B * T * 576 * 2
         nbytes = kv_bytes + B * H * 576 * 2 + ns * B * H * (512 * 2 + 4)
         flops = 2 * B * H * T * (576 + 512)
@@ -479,7 +482,9 @@ def mla_extras(hbm_peak, tensor_peak):
             "frac_of_measured_hbm": round(nbytes / us / 1e3 / hbm_peak, 4),
             "frac_of_measured_bf16_tensor": round(flops / us / 1e6 / tensor_peak, 4),
             "kernel": {dcp.DCP_MLA_KERNEL_TCGEN05: "tcgen05", dcp.DCP_MLA_KERNEL_MMA_SYNC: "mma.sync"}[
-                dcp.dcp_mla_decode_kernel(H, T, ns, dcp.DCP_FLAG_PDL)],
+                dcp.dcp_mla_decode_kernel(H, T, ns, pf)],
+            "launch": "PDL + L2 prefetch of Q and the first KV tile before the dependency wait",
+            "us_per_call_without_prefetch": round(us_nopf, 2),
             "mma_sync_kernel_us_per_call": round(us_mma, 2)}
         # fused: the same cache split over cp shards of T/cp tokens each
         Ts = T // cp
@@ -489,7 +494,7 @@ def mla_extras(hbm_peak, tensor_peak):
         fo = [torch.empty((B, H // cp, 512), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
         fl = [torch.empty((B, H // cp), dtype=torch.float32, device="cuda") for _ in range(cp)]
         us_f = timed(lambda k: dcp.mla_decode_dcp(q, shard_kvs[k], shard_lens, MLA_SCALE, n_split=n_split,
-                                                  workspace=ws, outs=fo, lse_outs=fl, flags=dcp.DCP_FLAG_PDL))
+                                                  workspace=ws, outs=fo, lse_outs=fl, flags=pf))
         # Its two launches apart. The producer's grid (cp*n_split slots of
         # Ts/n_split tokens x head blocks x rows) is that of one producer call
         # over the whole cache with cp*n_split splits, since shard j holds the
@@ -499,7 +504,7 @@ def mla_extras(hbm_peak, tensor_peak):
         pp = [torch.empty((B, H, 512), dtype=torch.bfloat16, device="cuda") for _ in range(n_src)]
         ppl = [torch.empty((B, H), dtype=torch.float32, device="cuda") for _ in range(n_src)]
         us_p = timed(lambda k: dcp.mla_decode_partial(q, kvs[k], lens, MLA_SCALE, n_split=n_src, outs=pp, lses=ppl,
-                                                      flags=dcp.DCP_FLAG_PDL))
+                                                      flags=pf))
         Hs = H // n_src
         m_dst = [fo[k // n_split].data_ptr() + (k % n_split) * Hs * 512 * 2 for k in range(n_src)]
         m_lout = [fl[k // n_split].data_ptr() + (k % n_split) * Hs * 4 for k in range(n_src)]
@@ -514,7 +519,7 @@ def mla_extras(hbm_peak, tensor_peak):
             "fused_minus_parts_us": round(us_f - us_p - us_m, 2),
             "how_split": "producer alone = one producer call over the whole cache with cp*n_split splits (the fused "
                          "launch's grid); merge alone = the merge over those partials with the fused layout; each "
-                         "timed like the fused call (ten calls per graph, PDL)"}
+                         "timed like the fused call (ten calls per graph, PDL; the producer with its L2 prefetch)"}
         del q, kvs, shard_kvs, po, pl, ws, fo, fl, pp, ppl
         torch.cuda.empty_cache()
     return out
@@ -887,7 +892,8 @@ def run_case(args):
     torch.cuda.set_device(dist_env()[2])
     dcp_build.build()
     if args.case == "mla":
-        # the producer on a DeepSeek-V2-shaped shard: 8 rows x 128 heads x 4096 tokens, 16 splits
+        # the producer on a DeepSeek-V2-shaped shard, as the bench times it: 8 rows x 128 heads x 4096
+        # tokens, 9 splits (one wave), PDL and the L2 prefetch
         from decode_context_mla_dcp_gb300.inputs import MLA_SCALE
         gen = torch.Generator(device="cuda")
         gen.manual_seed(0)
@@ -896,7 +902,7 @@ def run_case(args):
         kvs = [torch.randn((B, T, 576), generator=gen, device="cuda").to(torch.bfloat16) for _ in range(args.calls)]
         lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
         for kv in kvs:
-            dcp.mla_decode_partial(q, kv, lens, MLA_SCALE, n_split=16)
+            dcp.mla_decode_partial(q, kv, lens, MLA_SCALE, n_split=9, flags=dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH)
         torch.cuda.synchronize()
         print(f"case mla x {args.calls} calls done", flush=True)
         return 0

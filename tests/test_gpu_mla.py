@@ -4,8 +4,10 @@ over the whole context.
 
 Tolerances: partial outputs |gpu - ref| <= 1e-2 + 8e-3*|ref| (bf16
 probabilities and bf16 output rounding dominate: about 2^-9 relative each);
-LSEs |gpu - ref| <= 1e-4 * max(|ref|, 1) (fp32 scores accumulated over
-Dk <= 576 bf16 products, hardware exp2/log2 at ~2 ulp).
+LSEs |gpu - ref| <= 1e-5 * max(|ref|, 1), the merge's LSE tolerance (fp32
+scores accumulated over Dk <= 576 bf16 products, hardware exp2 at ~2 ulp,
+fp32 sums over the tokens; the worst error these tests record is printed at
+the end of the run).
 """
 import math
 
@@ -21,7 +23,7 @@ from tests.conftest import record_error
 pytestmark = pytest.mark.gpu
 
 ATOL, RTOL = 1e-2, 8e-3
-LSE_TOL = 1e-4
+LSE_TOL = 1e-5
 
 
 @pytest.fixture(scope="module", autouse=True)
