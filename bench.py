@@ -909,6 +909,8 @@ def run_case(args):
     cfg = CONFIGS[args.case]
     rows_list = [int(r) for r in args.rows.split(",")] if args.rows else list(cfg.rows)
     flags = dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH
+    if args.schedule == "lse_first":
+        flags |= dcp.DCP_FLAG_LSE_FIRST
     for rows in rows_list:
         inp = make_merge_inputs(cfg, rows, seed=0)
         Hl = cfg.H // cfg.cp
@@ -942,6 +944,8 @@ def main(argv=None):
                     help="profiling mode: plain calls of one config, no timing")
     ap.add_argument("--rows", default="", help="with --case: comma-separated row counts")
     ap.add_argument("--calls", type=int, default=3, help="with --case: calls per row count")
+    ap.add_argument("--schedule", choices=["default", "lse_first"], default="default",
+                    help="with --case (merge configs): the merge schedule")
     args = ap.parse_args(argv)
     if args.case:
         return run_case(args)
