@@ -495,6 +495,9 @@ def mla_extras(hbm_peak, tensor_peak):
         fl = [torch.empty((B, H // cp), dtype=torch.float32, device="cuda") for _ in range(cp)]
         us_f = timed(lambda k: dcp.mla_decode_dcp(q, shard_kvs[k], shard_lens, MLA_SCALE, n_split=n_split,
                                                   workspace=ws, outs=fo, lse_outs=fl, flags=pf))
+        us_f1 = timed(lambda k: dcp.mla_decode_dcp(q, shard_kvs[k], shard_lens, MLA_SCALE, n_split=n_split,
+                                                   workspace=ws, outs=fo, lse_outs=fl,
+                                                   flags=pf | dcp.DCP_MLA_FLAG_ONE_KERNEL))
         # Its two launches apart. The producer's grid (cp*n_split slots of
         # Ts/n_split tokens x head blocks x rows) is that of one producer call
         # over the whole cache with cp*n_split splits, since shard j holds the
@@ -515,6 +518,10 @@ def mla_extras(hbm_peak, tensor_peak):
         out[f"fused producer+merge, {name}"] = {
             "shape": f"B={B}, H={H}, cp={cp} shards x {Ts} tokens, n_split={n_split}", "us_per_call": round(us_f, 2),
             "kv_gbs": round(kv_bytes / us_f / 1e3, 1), "tflops": round(flops / us_f / 1e6, 1),
+            "launches": "two (producer, then the merge; PDL)",
+            "one_kernel_us_per_call": round(us_f1, 2),
+            "one_kernel": "DCP_MLA_FLAG_ONE_KERNEL: the merge inside the producer's cooperative launch after a "
+                          "grid-wide sync",
             "producer_alone_us": round(us_p, 2), "merge_alone_us": round(us_m, 2),
             "fused_minus_parts_us": round(us_f - us_p - us_m, 2),
             "how_split": "producer alone = one producer call over the whole cache with cp*n_split splits (the fused "

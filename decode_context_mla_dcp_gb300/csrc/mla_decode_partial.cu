@@ -27,6 +27,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <cooperative_groups.h>
 #include <mutex>
 
 #include "dcp_lse_reduce.h"
@@ -41,6 +42,7 @@ constexpr unsigned kFlagPdl = 1u;
 constexpr unsigned kFlagPrefetch = 8u;  // DCP_FLAG_PREFETCH: L2 prefetch of the first tile before the PDL wait
 constexpr unsigned kFlagMmaSync = 2u;   // DCP_MLA_FLAG_MMA_SYNC
 constexpr unsigned kFlagTcgen05 = 4u;   // DCP_MLA_FLAG_TCGEN05
+constexpr unsigned kFlagOneKernel = 16u;  // DCP_MLA_FLAG_ONE_KERNEL (dcp_mla_decode only)
 // When the tcgen05 kernel is the default. Its MMAs cost about the same per
 // instruction whatever the head block (N = 16, 32 or 64), so it pays off with
 // 64-head blocks from one full 128-token tile per (row, split), with 32-head
@@ -163,6 +165,27 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// Loads through L2 only (data other CTAs of this grid wrote).
+__device__ __forceinline__ float ld_cg_f32(const float* ptr) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+    return v;
+}
+__device__ __forceinline__ uint4 ld_cg_v4(const uint8_t* ptr) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr));
+    return v;
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -451,6 +474,15 @@ struct TcParams {
     float scale_log2;
     float lse_scale;
     int prefetch;                     // 1: bring Q and the first KV tile into L2 before the PDL wait
+    // The merge in the same launch (dcp_mla_decode when the grid is one wave,
+    // launched cooperatively): after a grid-wide sync every warp merges (row,
+    // head) units of the gridDim.x partials into destination r = h / Hl.
+    int merge;
+    int Hl;                           // heads per destination (H / cp)
+    float merge_lse_scale;            // LSE differences -> log2 units: 1 or log2(e)
+    float merge_log_scale;            // log2(sum) -> the LSE base: 1 or ln 2
+    uint8_t* dst[kSlots];             // destination r: [B, Hl, Dv] bf16
+    float* lse_out[kSlots];           // destination r's merged LSEs [B, Hl], or null
 };
 
 template <int kDk, int kNH>
@@ -562,6 +594,101 @@ __device__ __forceinline__ void cta_reduce_heads(float* v, int quad, int hb, int
         out[h] = kSum ? (a + b) + (c + d) : fmaxf(fmaxf(a, b), fmaxf(c, d));
     }
     __syncthreads();
+}
+
+
+// The merge of the fused decode, one warp per (row, head) unit, with the same
+// arithmetic in the same order as dcp_lse_reduce (so the two paths agree bit
+// for bit): m = max of the LSEs, e_j = 2^((l_j - m) * s) (0 for -inf), sum
+// over j in order, weights e_j / sum by one reciprocal, fp32 FMAs over the
+// sources in order j = 0.. (zero weights skipped), round to bf16; merged LSE
+// m + log2(sum) * (1 or ln 2), -inf when every source is -inf.
+constexpr int kMergeBatch = 8;  // sources whose payloads are in flight together
+
+__device__ __noinline__ void merge_partials(const TcParams& p, int64_t B) {
+    constexpr int kMaxSrc = kSlots;
+    const int lane = threadIdx.x & 31;
+    const int n_src = (int)gridDim.x;
+    const int wpc = (int)(blockDim.x >> 5);
+    const int64_t cta = ((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    const int64_t total = (int64_t)gridDim.x * gridDim.y * gridDim.z * wpc;
+    const int64_t units = B * p.H;
+    for (int64_t u = cta * wpc + (threadIdx.x >> 5); u < units; u += total) {
+        const int b = (int)(u / p.H), h = (int)(u - (int64_t)b * p.H);
+        const int64_t row = (int64_t)b * p.H + h;
+        float l[kMaxSrc], w[kMaxSrc];
+#pragma unroll
+        for (int j = 0; j < kMaxSrc; ++j) l[j] = (j < n_src) ? ld_cg_f32(p.lse[j] + row) : -INFINITY;
+        float mx[kMaxSrc];
+#pragma unroll
+        for (int j = 0; j < kMaxSrc; ++j) mx[j] = l[j];
+#pragma unroll
+        for (int half = kMaxSrc / 2; half >= 1; half /= 2)
+#pragma unroll
+            for (int j = 0; j < half; ++j) mx[j] = fmaxf(mx[j], mx[j + half]);
+        const float m = mx[0];
+        float merged = -INFINITY;
+        if (m == -INFINITY) {
+#pragma unroll
+            for (int j = 0; j < kMaxSrc; ++j) w[j] = 0.f;
+        } else {
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxSrc; ++j) {
+                const float e = (l[j] == -INFINITY) ? 0.f : ex2((l[j] - m) * p.merge_lse_scale);
+                w[j] = e;
+                sum += e;
+            }
+            const float inv = rcp(sum);
+#pragma unroll
+            for (int j = 0; j < kMaxSrc; ++j) w[j] *= inv;
+            merged = fmaf(lg2(sum), p.merge_log_scale, m);
+        }
+        float acc[2][8];
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[v][e] = 0.f;
+#pragma unroll
+        for (int jb = 0; jb < kMaxSrc; jb += kMergeBatch) {
+            if (jb >= n_src) break;
+            uint4 x[kMergeBatch][2];
+#pragma unroll
+            for (int j = 0; j < kMergeBatch; ++j)
+#pragma unroll
+                for (int v = 0; v < 2; ++v)
+                    x[j][v] = (jb + j < n_src && w[jb + j] != 0.f)
+                                  ? ld_cg_v4(p.out[jb + j] + row * (kDv * 2) + v * 512 + lane * 16)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int j = 0; j < kMergeBatch; ++j) {
+                const float wj = w[jb + j];
+                if (jb + j < n_src && wj != 0.f) {
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        const uint32_t q[4] = {x[j][v].x, x[j][v].y, x[j][v].z, x[j][v].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            acc[v][2 * e] = fmaf(wj, __uint_as_float(q[e] << 16), acc[v][2 * e]);
+                            acc[v][2 * e + 1] = fmaf(wj, __uint_as_float(q[e] & 0xffff0000u), acc[v][2 * e + 1]);
+                        }
+                    }
+                }
+            }
+        }
+        const int r = h / p.Hl, i = h - r * p.Hl;
+        uint8_t* const dst = p.dst[r] + ((int64_t)b * p.Hl + i) * (kDv * 2);
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            uint4 o;
+            o.x = pack_bf16(acc[v][0], acc[v][1]);
+            o.y = pack_bf16(acc[v][2], acc[v][3]);
+            o.z = pack_bf16(acc[v][4], acc[v][5]);
+            o.w = pack_bf16(acc[v][6], acc[v][7]);
+            *reinterpret_cast<uint4*>(dst + v * 512 + lane * 16) = o;
+        }
+        if (lane == 0 && p.lse_out[r] != nullptr) p.lse_out[r][(int64_t)b * p.Hl + i] = merged;
+    }
 }
 
 // Threads of the tcgen05 kernel: one per (token, group of heads); with 32 or
@@ -892,8 +1019,16 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
             if (tid < kNH) lse[(int64_t)b * p.H + h0 + tid] = (m_s[tid] + log2f(t_s[tid])) * p.lse_scale;
             // before the CTA leaves, the copy must have read the tile out of shared
             // memory (its global writes are visible to later kernels once this grid
-            // completes)
-            if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            // completes); when this grid merges the partials itself, the writes
+            // must be complete and ordered before the grid-wide sync
+            if (tid == 0) {
+                if (p.merge) {
+                    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                } else {
+                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                }
+            }
         }
     }
     if (aborted) {
@@ -913,6 +1048,14 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
     __syncthreads();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+    if (p.merge) {
+        // Every CTA reaches this point (each of its waits is bounded and an
+        // aborted CTA comes here too) and a cooperative launch keeps every CTA
+        // resident, so the grid-wide sync completes.
+        __threadfence();
+        cooperative_groups::this_grid().sync();
+        merge_partials(p, (int64_t)gridDim.z);
+    }
 }
 
 // ---- host side -----------------------------------------------------------------
@@ -999,12 +1142,49 @@ cudaError_t launch_tc(const TcParams& prm, int64_t B, int n_slots, unsigned flag
     cfg.blockDim = dim3(128 * tc_head_groups<kNH>(), 1, 1);
     cfg.dynamicSmemBytes = bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (flags & kFlagPdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (prm.merge) {  // the grid-wide sync needs every CTA resident at once
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = (flags & kFlagPdl) ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel<kDk, kNH>, prm);
+}
+
+// CTAs of the tcgen05 kernel that can be resident at once on the device (the
+// limit of a cooperative launch).
+template <int kDk, int kNH>
+int64_t tc_resident_ctas() {
+    constexpr int bytes = tc_smem_bytes<kDk, kNH>();
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (cudaFuncSetAttribute(mla_partial_tc_kernel<kDk, kNH>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mla_partial_tc_kernel<kDk, kNH>,
+                                                      128 * tc_head_groups<kNH>(), bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return (int64_t)sms * per_sm;
+}
+
+template <int kDk>
+int64_t tc_resident_ctas_dk(int H) {
+    if (H % 64 == 0) return tc_resident_ctas<kDk, 64>();
+    if (H % 32 == 0) return tc_resident_ctas<kDk, 32>();
+    return tc_resident_ctas<kDk, 16>();
 }
 
 template <int kDk>
@@ -1080,9 +1260,20 @@ bool shape_ok(int64_t B, int H, int Dk, int Dv, int64_t T) {
 
 // Validate and launch the producer over n_shard shards x n_split splits
 // (slot = shard * n_split + split), all in one grid.
+// The merge a producer launch may finish with (dcp_mla_decode): cp
+// destinations of H / cp heads each.
+struct MergeInto {
+    void* const* dst;
+    float* const* lse_out;
+    int cp;
+};
+
+// 1 if the producer ran and merged (out == 1), 0 if it ran without merging.
 int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv_len_ptrs, int n_shard, int64_t B,
              int H, int Dk, int Dv, int64_t T, float scale, int lse_base_e, int n_split, void* const* out_ptrs,
-             float* const* lse_ptrs, int32_t* status, unsigned flags, void* stream) {
+             float* const* lse_ptrs, int32_t* status, unsigned flags, void* stream, const MergeInto* merge = nullptr,
+             int* merged = nullptr) {
+    if (merged != nullptr) *merged = 0;
     if (q == nullptr || kv_ptrs == nullptr || kv_len_ptrs == nullptr || out_ptrs == nullptr || lse_ptrs == nullptr)
         return DCP_MLA_ERR_NULL_POINTER;
     if (!shape_ok(B, H, Dk, Dv, T)) return DCP_MLA_ERR_BAD_SHAPE;
@@ -1137,12 +1328,36 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
         tp.scale_log2 = scale * 1.4426950408889634f;
         tp.lse_scale = lse_base_e ? 0.6931471805599453f : 1.0f;
         tp.prefetch = (flags & kFlagPrefetch) ? 1 : 0;
+        tp.merge = 0;
+        tp.Hl = H;
+        tp.merge_lse_scale = lse_base_e ? 1.4426950408889634f : 1.0f;
+        tp.merge_log_scale = lse_base_e ? 0.6931471805599453f : 1.0f;
+        for (int j = 0; j < kSlots; ++j) {
+            tp.dst[j] = nullptr;
+            tp.lse_out[j] = nullptr;
+        }
+        // The merge joins this launch when the grid fits in one resident wave
+        // (a cooperative launch then keeps every CTA resident for the grid-wide
+        // sync); otherwise the caller launches the merge separately.
+        if (merge != nullptr) {
+            const int64_t ctas = (int64_t)n_slots * (H / (H % 64 == 0 ? 64 : (H % 32 == 0 ? 32 : 16))) * B;
+            const int64_t resident = Dk == 576 ? tc_resident_ctas_dk<576>(H) : tc_resident_ctas_dk<512>(H);
+            if (ctas <= resident && merge->cp <= kSlots) {
+                tp.merge = 1;
+                tp.Hl = H / merge->cp;
+                for (int j = 0; j < merge->cp; ++j) {
+                    tp.dst[j] = static_cast<uint8_t*>(merge->dst[j]);
+                    tp.lse_out[j] = merge->lse_out != nullptr ? merge->lse_out[j] : nullptr;
+                }
+            }
+        }
         const cudaError_t e = Dk == 576 ? launch_tc_dk<576>(tp, B, n_slots, flags & kFlagPdl, st)
                                         : launch_tc_dk<512>(tp, B, n_slots, flags & kFlagPdl, st);
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             return (int)e;
         }
+        if (merged != nullptr) *merged = tp.merge;
         return 0;
     }
     prm.q = static_cast<const uint8_t*>(q);
@@ -1208,9 +1423,19 @@ extern "C" int dcp_mla_decode(const void* q, const void* const* kv_ptrs, const i
         part_out[k] = ws + k * out_bytes;
         part_lse[k] = reinterpret_cast<float*>(ws + n_src * out_bytes + k * lse_bytes);
     }
+    // With DCP_MLA_FLAG_ONE_KERNEL, and when the producer's grid is one wave of
+    // tcgen05 CTAs, the merge runs in the producer's launch after a grid-wide
+    // sync; otherwise the producer and the merge are two launches.
+    const bool one = (flags & kFlagOneKernel) != 0;
+    for (int j = 0; j < cp; ++j)
+        if (!aligned(dst_ptrs[j], 16) || (lse_out_ptrs != nullptr && lse_out_ptrs[j] != nullptr &&
+                                          !aligned(lse_out_ptrs[j], 4)))
+            return DCP_MLA_ERR_MISALIGNED;
+    const MergeInto into{dst_ptrs, lse_out_ptrs, cp};
+    int merged = 0;
     int rc = producer(q, kv_ptrs, kv_len_ptrs, cp, B, H, Dk, Dv, T, scale, lse_base_e, n_split, part_out, part_lse,
-                      status, flags, stream);
-    if (rc != 0 || B == 0) return rc;
+                      status, flags & ~kFlagOneKernel, stream, one ? &into : nullptr, &merged);
+    if (rc != 0 || B == 0 || merged) return rc;
 
     // Merge source k into head block k of width H/n_src: block k lies in
     // destination k / n_split at local head (k % n_split) * H/n_src.

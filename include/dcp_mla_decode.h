@@ -71,8 +71,9 @@ enum {
     DCP_MLA_ERR_BAD_SPLIT = -103,    /* n_split outside [1, DCP_MLA_SPLIT_MAX] */
     DCP_MLA_ERR_MISALIGNED = -104,   /* q, kv or an output not 16-byte aligned, or an LSE or kv_len
                                         pointer not 4-byte aligned */
-    DCP_MLA_ERR_BAD_FLAGS = -105,    /* unknown flag bits (DCP_FLAG_PDL, DCP_FLAG_PREFETCH and the two below
-                                        are known), or both DCP_MLA_FLAG_MMA_SYNC and DCP_MLA_FLAG_TCGEN05 */
+    DCP_MLA_ERR_BAD_FLAGS = -105,    /* unknown flag bits (DCP_FLAG_PDL, DCP_FLAG_PREFETCH and the flags
+                                        below are known; DCP_MLA_FLAG_ONE_KERNEL only by dcp_mla_decode),
+                                        or both DCP_MLA_FLAG_MMA_SYNC and DCP_MLA_FLAG_TCGEN05 */
     DCP_MLA_ERR_WORKSPACE = -106,    /* workspace NULL, not 256-byte aligned, or smaller than
                                         dcp_mla_decode_workspace_bytes(...) */
     DCP_MLA_ERR_BAD_CP = -107,       /* cp < 1, cp*n_split > 16, or H not a multiple of cp*n_split */
@@ -93,6 +94,12 @@ enum {
  */
 #define DCP_MLA_FLAG_MMA_SYNC 2u
 #define DCP_MLA_FLAG_TCGEN05 4u
+/*
+ * dcp_mla_decode only: run the merge inside the producer's launch where the
+ * tcgen05 grid fits one wave (see dcp_mla_decode). Slower on GB300 than the
+ * default two launches with PDL, so off by default.
+ */
+#define DCP_MLA_FLAG_ONE_KERNEL 16u
 /*
  * DCP_FLAG_PREFETCH (8, include/dcp_lse_reduce.h) is also taken by the
  * producer: each CTA of the tcgen05 kernel brings Q and its split's first KV
@@ -164,11 +171,22 @@ int64_t dcp_mla_decode_workspace_bytes(int cp, int n_split, int64_t B, int H, in
  * shards' tokens): "[DCP] Optimize shared Output, Query, and Indexer/Top-K via
  * peer memory" (sglang #32851), commit notes on the interleaved KV shards and
  * the cross-rank combine; on one GPU the shards are local buffers and the
- * exchange is the merge's strided read. One launch of the producer (covering
- * every shard and split) and one merge are enqueued on `stream` (PDL between
- * them with DCP_FLAG_PDL); the producer kernel per dcp_mla_decode_kernel(H,
- * T, n_split, flags).
- * Constraints: cp*n_split <= 16 and H a multiple of cp*n_split and of 16.
+ * exchange is the merge's strided read. The producer kernel is the one
+ * dcp_mla_decode_kernel(H, T, n_split, flags) names, in one launch covering
+ * every shard and split.
+ *   - By default the merge is a second launch (PDL between the two with
+ *     DCP_FLAG_PDL).
+ *   - With DCP_MLA_FLAG_ONE_KERNEL, when the producer is the tcgen05 kernel
+ *     and its grid (cp * n_split * head blocks * B CTAs) fits in one resident
+ *     wave, the merge runs in the same launch instead: a cooperative launch,
+ *     in which every CTA writes its partial to the workspace, the grid
+ *     synchronises once, and every warp then merges (row, head) units into
+ *     the destinations. On GB300 this measured slower than the two launches
+ *     (the cooperative launch and the grid-wide sync cost more than the
+ *     second launch and its gap under PDL); it is kept for comparison.
+ *   Both give bit-identical results (the same arithmetic in the same order).
+ * Constraints: cp*n_split <= 16 and H a multiple of cp*n_split and of 16;
+ * dst_ptrs 16-byte and lse_out_ptrs 4-byte aligned (DCP_MLA_ERR_MISALIGNED).
  */
 int dcp_mla_decode(const void* q, const void* const* kv_ptrs, const int32_t* const* kv_len_ptrs, int cp,
                    int64_t B, int H, int Dk, int Dv, int64_t T, float scale, int lse_base_e, int n_split,

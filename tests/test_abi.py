@@ -130,7 +130,7 @@ def test_mla_producer_rejects_bad_arguments(lib):
     assert call(Dk=640) == -102 and call(Dv=256) == -102 and call(T=-1) == -102
     assert call(n_split=0) == -103 and call(n_split=17) == -103
     assert call(q=FAKE + 8) == -104 and call(kv_len=FAKE + 2) == -104 and call(o=arr(FAKE + 4, FAKE)) == -104
-    assert call(flags=16) == -105 and call(flags=6) == -105
+    assert call(flags=16) == -105 and call(flags=6) == -105  # the one-kernel flag is dcp_mla_decode's only
     assert call(flags=dcp.DCP_FLAG_PREFETCH | dcp.DCP_FLAG_PDL, B=0) == 0  # the producer takes the prefetch flag
     assert call(B=0) == 0  # nothing to do, nothing launched
     assert dcp.dcp_mla_decode_smem_bytes(576, 64) > 150000
@@ -244,3 +244,9 @@ def test_no_alloc_reports_bad_shapes_before_the_scratch_limit(lib):
     assert noalloc(n_split=17) == -103 and noalloc(cp=16) == -107
     assert fused(Dv=4096) == -102 and fused(B=-1) == -102
     assert fused() == -106                        # valid shape, workspace too small
+    need = dcp.dcp_mla_decode_workspace_bytes(8, 2, 0, 128)
+    assert fused(B=0, ws_bytes=1 << 20, ) == 0 and need == 0
+    assert lib.dcp_mla_decode(FAKE, ptrs, ptrs, 8, 0, 128, 576, 512, 100, 0.1, 1, 2, FAKE, 1 << 20, ptrs, None, None,
+                              dcp.DCP_MLA_FLAG_ONE_KERNEL | dcp.DCP_FLAG_PDL, None) == 0
+    assert lib.dcp_mla_decode(FAKE, ptrs, ptrs, 8, 0, 128, 576, 512, 100, 0.1, 1, 2, FAKE, 1 << 20, ptrs, None, None,
+                              32, None) == -105

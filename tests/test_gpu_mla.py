@@ -430,3 +430,73 @@ def test_picked_split_count_in_the_python_wrappers():
     torch.cuda.synchronize()
     assert all(torch.equal(x, y) for x, y in zip(a, b)) and all(torch.equal(x, y) for x, y in zip(al, bl))
     assert len(po) == dcp.dcp_mla_decode_pick_split(1, B, H, T, sms)
+
+
+@pytest.mark.parametrize("cp,n_split,H,B,L_max,base_e", [(8, 1, 128, 8, 4096, True), (4, 4, 64, 8, 4096, False),
+                                                         (4, 2, 64, 3, 1100, True), (2, 1, 128, 5, 600, True)])
+def test_one_kernel_decode_equals_two_launches_bit_for_bit(cp, n_split, H, B, L_max, base_e):
+    """With DCP_MLA_FLAG_ONE_KERNEL dcp_mla_decode merges inside the
+    producer's launch (one cooperative launch, a grid-wide sync, then every
+    warp merges) when the tcgen05 grid fits one wave; by default the merge is
+    its own launch. Same arithmetic in the same order: identical bits,
+    including rows whose shards are partly or wholly empty."""
+    q, kv_full = make_mla_inputs(B, H, L_max, 576, seed=cp * 1000 + H + B)
+    L = np.full(B, L_max, dtype=np.int32)
+    L[1] = L_max // 3
+    L[2] = cp - 1  # one shard empty
+    if B > 3:
+        L[3] = 0   # every shard empty
+    kvs, lens = _interleaved_shards(kv_full, L, cp)
+    T = kvs[0].shape[1]
+    tc = dcp.DCP_MLA_FLAG_TCGEN05
+    assert dcp.dcp_mla_decode_kernel(H, T, n_split, tc) == dcp.DCP_MLA_KERNEL_TCGEN05
+    qd = dev_bf16(q)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o1, l1 = dcp.mla_decode_dcp(qd, kvs, lens, MLA_SCALE, n_split=n_split, lse_base_e=base_e, status=status,
+                                flags=tc | dcp.DCP_FLAG_PDL | dcp.DCP_MLA_FLAG_ONE_KERNEL)
+    o2, l2 = dcp.mla_decode_dcp(qd, kvs, lens, MLA_SCALE, n_split=n_split, lse_base_e=base_e, status=status,
+                                flags=tc | dcp.DCP_FLAG_PDL)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for r in range(cp):
+        assert torch.equal(o1[r].view(torch.int16), o2[r].view(torch.int16)), f"destination {r} output"
+        assert torch.equal(l1[r].view(torch.int32), l2[r].view(torch.int32)), f"destination {r} LSE"
+    if B > 3:
+        assert all(bool((o[3] == 0).all()) and bool((l[3] == -float("inf")).all()) for o, l in zip(o1, l1))
+
+
+def test_one_kernel_decode_matches_attention_and_replays_in_a_graph(oracle_mod):
+    from oracle.attention import attention
+    B, H, L_max, cp, n_split = 3, 64, 900, 4, 1
+    q, kv_full = make_mla_inputs(B, H, L_max, 576, seed=77)
+    L = np.array([900, 513, 129], dtype=np.int32)
+    kvs, lens = _interleaved_shards(kv_full, L, cp)
+    qd = dev_bf16(q)
+    flags = dcp.DCP_MLA_FLAG_TCGEN05 | dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH | dcp.DCP_MLA_FLAG_ONE_KERNEL
+    ws = torch.empty((dcp.dcp_mla_decode_workspace_bytes(cp, n_split, B, H),), dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((B, H // cp, 512), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
+    louts = [torch.empty((B, H // cp), dtype=torch.float32, device="cuda") for _ in range(cp)]
+
+    def call():
+        dcp.mla_decode_dcp(qd, kvs, lens, MLA_SCALE, n_split=n_split, workspace=ws, outs=outs, lse_outs=louts,
+                           flags=flags)
+
+    call()
+    torch.cuda.synchronize()
+    Hl = H // cp
+    for b in range(B):
+        o_ref, l_ref = attention(widen(q[b:b + 1]), widen(kv_full[b, :L[b]]), MLA_SCALE, dv=512)
+        for r in range(cp):
+            check_out(outs[r][b:b + 1], o_ref[:, r * Hl:(r + 1) * Hl], f"row {b} dest {r}", kind="fused decode")
+            check_lse(louts[r][b:b + 1], l_ref[:, r * Hl:(r + 1) * Hl], f"row {b} dest {r}", kind="fused decode")
+    ref = [o.clone() for o in outs] + [l.clone() for l in louts]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+        call()
+    for t in outs + louts:
+        t.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(ref, outs + louts))
