@@ -17,6 +17,7 @@ from __future__ import annotations
 from ._binding import (DCP_DTYPE_BF16, DCP_DTYPE_F16, DCP_FLAG_LSE_FIRST, DCP_FLAG_PDL, DCP_FLAG_PRELOAD,
                        DCP_FLAG_PREFETCH,
                        DCP_LSE_REDUCE_CP_MAX, DCP_MLA_FLAG_MMA_SYNC, DCP_MLA_FLAG_TCGEN05, DCP_MLA_FLAG_ONE_KERNEL,
+                       DCP_MLA_FLAG_TEST_STALL,
                        DCP_MLA_SPLIT_MAX,
                        DCP_MLA_KERNEL_MMA_SYNC, DCP_MLA_KERNEL_TCGEN05, dcp_mla_decode_kernel,
                        dcp_mla_decode_pick_split,
@@ -31,7 +32,7 @@ __all__ = ["dcp_lse_reduce", "dcp_lse_reduce_ex", "dcp_lse_reduce_strerror", "dc
            "dcp_mla_decode_partial", "dcp_mla_decode_smem_bytes", "mla_decode_partial", "DCP_MLA_SPLIT_MAX",
            "dcp_mla_decode", "dcp_mla_decode_workspace_bytes", "mla_decode_dcp", "dcp_mla_decode_noalloc",
            "DCP_MLA_NOALLOC_SCRATCH_BYTES", "DCP_MLA_FLAG_MMA_SYNC", "DCP_MLA_FLAG_TCGEN05",
-           "DCP_MLA_FLAG_ONE_KERNEL",
+           "DCP_MLA_FLAG_ONE_KERNEL", "DCP_MLA_FLAG_TEST_STALL",
            "algorithmic_bytes", "Layout", "DcpError", "load", "library_path", "EXPORTED_SYMBOLS",
            "DCP_DTYPE_BF16", "DCP_DTYPE_F16", "DCP_FLAG_PDL", "DCP_FLAG_PRELOAD", "DCP_FLAG_LSE_FIRST",
            "DCP_FLAG_PREFETCH",

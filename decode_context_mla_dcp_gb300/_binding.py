@@ -31,6 +31,7 @@ DCP_MLA_SPLIT_MAX = 16
 DCP_MLA_FLAG_MMA_SYNC = 2
 DCP_MLA_FLAG_TCGEN05 = 4
 DCP_MLA_FLAG_ONE_KERNEL = 16
+DCP_MLA_FLAG_TEST_STALL = 32
 DCP_MLA_KERNEL_TCGEN05 = 1
 DCP_MLA_KERNEL_MMA_SYNC = 2
 DCP_LSE_REDUCE_INTERLEAVE_MAX = 1 << 24

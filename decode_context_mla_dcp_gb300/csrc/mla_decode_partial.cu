@@ -43,6 +43,7 @@ constexpr unsigned kFlagPrefetch = 8u;  // DCP_FLAG_PREFETCH: L2 prefetch of the
 constexpr unsigned kFlagMmaSync = 2u;   // DCP_MLA_FLAG_MMA_SYNC
 constexpr unsigned kFlagTcgen05 = 4u;   // DCP_MLA_FLAG_TCGEN05
 constexpr unsigned kFlagOneKernel = 16u;  // DCP_MLA_FLAG_ONE_KERNEL (dcp_mla_decode only)
+constexpr unsigned kFlagTestStall = 32u;  // DCP_MLA_FLAG_TEST_STALL
 // When the tcgen05 kernel is the default. Its MMAs cost about the same per
 // instruction whatever the head block (N = 16, 32 or 64), so it pays off with
 // 64-head blocks from one full 128-token tile per (row, split), with 32-head
@@ -50,7 +51,8 @@ constexpr unsigned kFlagOneKernel = 16u;  // DCP_MLA_FLAG_ONE_KERNEL (dcp_mla_de
 // faster at every measured length.
 constexpr int64_t kTcMinTokensH64 = 128;
 constexpr int64_t kTcMinTokensH32 = 256;
-constexpr long long kWaitLimitNs = 2000000000LL;
+constexpr long long kWaitLimitNs = 2000000000LL;      // every wait of a call gives up after this
+constexpr long long kTestWaitLimitNs = 20000000LL;    // ... or this, with DCP_MLA_FLAG_TEST_STALL
 
 constexpr int kSlots = 16;            // (shard, split) outputs of one launch
 
@@ -65,6 +67,8 @@ struct Params {
     int H, n_split;
     float scale_log2;                 // softmax scale * log2(e): scores in base-2 units
     float lse_scale;                  // ln 2 for a natural-log LSE, 1 for base 2
+    long long wait_ns;                // limit of every wait (kWaitLimitNs, or kTestWaitLimitNs)
+    int stall;                        // DCP_MLA_FLAG_TEST_STALL: the first tile's barrier expects 16 bytes more
 };
 
 template <int kDk>
@@ -109,18 +113,19 @@ __device__ __forceinline__ long long global_ns() {
 }
 // The waits of both kernels. Every thread of a CTA shares one abort
 // flag in shared memory: a wait that has not seen its phase after
-// kWaitLimitNs sets it (and ORs 1 into the status word), and from then on
+// limit_ns (the call's wait limit) sets it (and ORs 1 into the status word), and from then on
 // every wait of the CTA returns at once. Returns whether the phase completed.
 // The kernel stops issuing copies and MMAs, leaves its tile loop at the next
 // tile boundary (a barrier vote, so all threads leave together), skips the
 // epilogue (the outputs are not valid) and drains the copies and MMAs it
 // armed before it frees TMEM and exits.
-__device__ __forceinline__ bool mbar_wait_cta(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
+__device__ __forceinline__ bool mbar_wait_cta(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                              long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             if (status != nullptr) atomicOr(status, 1);
             return false;
@@ -129,11 +134,11 @@ __device__ __forceinline__ bool mbar_wait_cta(uint64_t* bar, uint32_t parity, vo
     return true;
 }
 // Bounded wait that ignores the abort flag: the drain before TMEM is freed.
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     return true;
 }
 // One contiguous global -> shared copy by the bulk-copy engine.
@@ -267,7 +272,8 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
     auto load_tile = [&](int i, int buf) {
         const int rows = (ntok - i * kNt) < kNt ? (ntok - i * kNt) : kNt;
         uint8_t* dst = kv_s + buf * kNt * kRow;
-        mbar_expect_tx(&bars[1 + buf], (uint32_t)(rows * kDk * 2));
+        // (with the stall test, tile 0's barrier waits for 16 bytes that never come)
+        mbar_expect_tx(&bars[1 + buf], (uint32_t)(rows * kDk * 2) + (p.stall && i == 0 ? 16u : 0u));
         for (int r = 0; r < rows; ++r)
             bulk_g2s(dst + r * kRow, kv_row + ((int64_t)i * kNt + r) * kDk * 2, kDk * 2, &bars[1 + buf]);
         armed[buf] = i;
@@ -279,7 +285,7 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
         load_tile(0, 0);
         if (ntiles > 1) load_tile(1, 1);
     }
-    (void)mbar_wait_cta(&bars[0], 0, abort_flag, p.status);
+    (void)mbar_wait_cta(&bars[0], 0, abort_flag, p.status, p.wait_ns);
 
     // per-lane state: rows gr and gr+8 of the warp's 16 heads
     float m_run[2] = {-INFINITY, -INFINITY};  // running max, base-2 units
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
     bool aborted = false;  // CTA-uniform: decided by a barrier vote at the end of each tile
     for (int i = 0; i < ntiles; ++i) {
         const int buf = i & 1;
-        (void)mbar_wait_cta(&bars[1 + buf], (uint32_t)((i >> 1) & 1), abort_flag, p.status);
+        (void)mbar_wait_cta(&bars[1 + buf], (uint32_t)((i >> 1) & 1), abort_flag, p.status, p.wait_ns);
         const uint32_t kt = smem_u32(kv_s + buf * kNt * kRow);
 
         // partial scores: 16 heads x 16 tokens over half of Dk
@@ -414,9 +420,9 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
     }
     if (aborted) {  // outputs not valid (status says so); no copy may still land in shared memory
         if (threadIdx.x == 0) {
-            (void)mbar_wait_drain(&bars[0], 0);
+            (void)mbar_wait_drain(&bars[0], 0, p.wait_ns);
             for (int k = 0; k < 2; ++k)
-                if (armed[k] >= 0) (void)mbar_wait_drain(&bars[1 + k], (uint32_t)((armed[k] >> 1) & 1));
+                if (armed[k] >= 0) (void)mbar_wait_drain(&bars[1 + k], (uint32_t)((armed[k] >> 1) & 1), p.wait_ns);
         }
         return;
     }
@@ -474,6 +480,8 @@ struct TcParams {
     float scale_log2;
     float lse_scale;
     int prefetch;                     // 1: bring Q and the first KV tile into L2 before the PDL wait
+    long long wait_ns;                // limit of every wait (kWaitLimitNs, or kTestWaitLimitNs)
+    int stall;                        // DCP_MLA_FLAG_TEST_STALL: the first tile's barrier expects 16 bytes more
     // The merge in the same launch (dcp_mla_decode when the grid is one wave,
     // launched cooperatively): after a grid-wide sync every warp merges (row,
     // head) units of the gridDim.x partials into destination r = h / Hl.
@@ -803,14 +811,15 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
             mbar_expect_tx(bar_q, (uint32_t)(kAtoms * kQAtom));
             for (int a = 0; a < kAtoms; ++a) tma_load_2d(q_s + a * kQAtom, &p.tm_q, a * 64, b * p.H + h0, bar_q);
             armed[kArmQ] = 0;
-            mbar_expect_tx(bar_kv, (uint32_t)(kAtoms * kTcAtom));
+            // (with the stall test, the first tile's barrier waits for 16 bytes that never come)
+            mbar_expect_tx(bar_kv, (uint32_t)(kAtoms * kTcAtom) + (p.stall ? 16u : 0u));
             for (int a = 0; a < kAtoms; ++a) tma_load_2d(kv_s + a * kTcAtom, &p.tm_kv[shard], a * 64, row0, bar_kv);
             armed[kArmKv] = 0;
         }
         float l_part[kHW];  // this thread's token's share of each of its heads' sums
 #pragma unroll
         for (int h = 0; h < kHW; ++h) l_part[h] = 0.f;
-        (void)mbar_wait_cta(bar_q, 0, abort_flag, p.status);
+        (void)mbar_wait_cta(bar_q, 0, abort_flag, p.status, p.wait_ns);
 
         for (int i = 0; i < ntiles; ++i) {
             // Stop at a tile boundary, all threads together, once any wait gave up.
@@ -819,7 +828,7 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
                 break;
             }
             const uint32_t ph = (uint32_t)(i & 1);
-            (void)mbar_wait_cta(bar_kv, ph, abort_flag, p.status);
+            (void)mbar_wait_cta(bar_kv, ph, abort_flag, p.status, p.wait_ns);
             // Start the next tile's DRAM reads now, into L2 (from a thread of another
             // warp than the MMA issuer's), so that its load after this tile's value
             // MMAs streams from L2: every CTA reloads at about the same moment, and
@@ -840,7 +849,7 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
                 umma_commit(bar_s);
                 armed[kArmS] = i;
             }
-            (void)mbar_wait_cta(bar_s, ph, abort_flag, p.status);
+            (void)mbar_wait_cta(bar_s, ph, abort_flag, p.status, p.wait_ns);
             tc_fence_after();
 
             float sv[kHW];
@@ -889,7 +898,7 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
                 __syncthreads();
             }
             if (any && i > 0) {  // rescale O^T (the previous tile's value MMAs are done)
-                (void)mbar_wait_cta(bar_o, (uint32_t)((i - 1) & 1), abort_flag, p.status);
+                (void)mbar_wait_cta(bar_o, (uint32_t)((i - 1) & 1), abort_flag, p.status, p.wait_ns);
                 tc_fence_after();
 #pragma unroll 1
                 for (int m = 0; m < 4; ++m) {
@@ -962,7 +971,7 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
                 umma_commit(bar_o);
                 armed[kArmO] = i;
                 // the next tile reuses every buffer once these MMAs are done
-                if (i + 1 < ntiles && mbar_wait_cta(bar_o, ph, abort_flag, p.status)) {
+                if (i + 1 < ntiles && mbar_wait_cta(bar_o, ph, abort_flag, p.status, p.wait_ns)) {
                     mbar_expect_tx(bar_kv, (uint32_t)(kAtoms * kTcAtom));
                     for (int a = 0; a < kAtoms; ++a)
                         tma_load_2d(kv_s + a * kTcAtom, &p.tm_kv[shard], a * 64, row0 + (i + 1) * kTcTok, bar_kv);
@@ -973,7 +982,7 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
 
         if (!aborted) {
             // final sums, then normalise, round to bf16 and store; LSE = m + log2(l)
-            (void)mbar_wait_cta(bar_o, (uint32_t)((ntiles - 1) & 1), abort_flag, p.status);
+            (void)mbar_wait_cta(bar_o, (uint32_t)((ntiles - 1) & 1), abort_flag, p.status, p.wait_ns);
             aborted = __syncthreads_or(*abort_flag != 0) != 0;
         }
         if (!aborted) {
@@ -1038,10 +1047,10 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
         // TMEM.
         __syncthreads();
         if (tid == 0) {
-            if (armed[kArmQ] >= 0) (void)mbar_wait_drain(bar_q, 0);
-            if (armed[kArmKv] >= 0) (void)mbar_wait_drain(bar_kv, (uint32_t)(armed[kArmKv] & 1));
-            if (armed[kArmS] >= 0) (void)mbar_wait_drain(bar_s, (uint32_t)(armed[kArmS] & 1));
-            if (armed[kArmO] >= 0) (void)mbar_wait_drain(bar_o, (uint32_t)(armed[kArmO] & 1));
+            if (armed[kArmQ] >= 0) (void)mbar_wait_drain(bar_q, 0, p.wait_ns);
+            if (armed[kArmKv] >= 0) (void)mbar_wait_drain(bar_kv, (uint32_t)(armed[kArmKv] & 1), p.wait_ns);
+            if (armed[kArmS] >= 0) (void)mbar_wait_drain(bar_s, (uint32_t)(armed[kArmS] & 1), p.wait_ns);
+            if (armed[kArmO] >= 0) (void)mbar_wait_drain(bar_o, (uint32_t)(armed[kArmO] & 1), p.wait_ns);
         }
     }
     tc_fence_before();
@@ -1219,7 +1228,8 @@ bool tc_is_default(int H, int64_t tokens_per_split) {
 extern "C" int dcp_mla_decode_kernel(int H, int64_t T, int n_split, unsigned flags) {
     if (H < 16 || H % 16 != 0 || T < 0) return DCP_MLA_ERR_BAD_SHAPE;
     if (n_split < 1 || n_split > DCP_MLA_SPLIT_MAX) return DCP_MLA_ERR_BAD_SPLIT;
-    if ((flags & ~(kFlagPdl | kFlagPrefetch | kFlagMmaSync | kFlagTcgen05)) != 0) return DCP_MLA_ERR_BAD_FLAGS;
+    if ((flags & ~(kFlagPdl | kFlagPrefetch | kFlagMmaSync | kFlagTcgen05 | kFlagTestStall)) != 0)
+        return DCP_MLA_ERR_BAD_FLAGS;
     if ((flags & kFlagMmaSync) && (flags & kFlagTcgen05)) return DCP_MLA_ERR_BAD_FLAGS;
     if (flags & kFlagTcgen05) return DCP_MLA_KERNEL_TCGEN05;
     if (flags & kFlagMmaSync) return DCP_MLA_KERNEL_MMA_SYNC;
@@ -1279,7 +1289,8 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
     if (!shape_ok(B, H, Dk, Dv, T)) return DCP_MLA_ERR_BAD_SHAPE;
     if (n_split < 1 || n_split > DCP_MLA_SPLIT_MAX) return DCP_MLA_ERR_BAD_SPLIT;
     if (n_shard < 1 || n_shard * n_split > kSlots) return DCP_MLA_ERR_BAD_CP;
-    if ((flags & ~(kFlagPdl | kFlagPrefetch | kFlagMmaSync | kFlagTcgen05)) != 0) return DCP_MLA_ERR_BAD_FLAGS;
+    if ((flags & ~(kFlagPdl | kFlagPrefetch | kFlagMmaSync | kFlagTcgen05 | kFlagTestStall)) != 0)
+        return DCP_MLA_ERR_BAD_FLAGS;
     if ((flags & kFlagMmaSync) && (flags & kFlagTcgen05)) return DCP_MLA_ERR_BAD_FLAGS;
     if (!aligned(q, 16) || (status != nullptr && !aligned(status, 4))) return DCP_MLA_ERR_MISALIGNED;
     Params prm;
@@ -1328,6 +1339,8 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
         tp.scale_log2 = scale * 1.4426950408889634f;
         tp.lse_scale = lse_base_e ? 0.6931471805599453f : 1.0f;
         tp.prefetch = (flags & kFlagPrefetch) ? 1 : 0;
+        tp.wait_ns = (flags & kFlagTestStall) ? kTestWaitLimitNs : kWaitLimitNs;
+        tp.stall = (flags & kFlagTestStall) ? 1 : 0;
         tp.merge = 0;
         tp.Hl = H;
         tp.merge_lse_scale = lse_base_e ? 1.4426950408889634f : 1.0f;
@@ -1367,6 +1380,8 @@ int producer(const void* q, const void* const* kv_ptrs, const int32_t* const* kv
     prm.n_split = n_split;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.lse_scale = lse_base_e ? 0.6931471805599453f : 1.0f;
+    prm.wait_ns = (flags & kFlagTestStall) ? kTestWaitLimitNs : kWaitLimitNs;
+    prm.stall = (flags & kFlagTestStall) ? 1 : 0;
     const cudaError_t e = Dk == 576 ? launch_dk<576>(prm, B, n_slots, flags & kFlagPdl, st)
                                     : launch_dk<512>(prm, B, n_slots, flags & kFlagPdl, st);
     if (e != cudaSuccess) {

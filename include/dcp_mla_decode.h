@@ -43,7 +43,8 @@
  *            16-byte aligned
  *   lse_ptrs host array of n_split device pointers, each [B, H] fp32
  *   status   NULL, or a device int32 the kernel ORs 1 into if a wait for its
- *            own asynchronous copies or MMAs ever exceeds two seconds. Then
+ *            own asynchronous copies or MMAs ever exceeds two seconds (20 ms
+ *            with DCP_MLA_FLAG_TEST_STALL). Then
  *            the CTA stops issuing copies and MMAs, leaves at the next tile
  *            boundary without writing its outputs (they are not valid), waits
  *            (again at most two seconds each) for what it had issued, frees
@@ -100,6 +101,17 @@ enum {
  * default two launches with PDL, so off by default.
  */
 #define DCP_MLA_FLAG_ONE_KERNEL 16u
+/*
+ * For tests of the bounded waits only: every CTA arms the barrier of its
+ * first KV tile for 16 bytes more than its copies deliver, so that wait never
+ * completes, and every wait of the call gives up after 20 ms instead of two
+ * seconds. The call then follows the protocol described under `status`: the
+ * status word reads 1 when the call has run on its stream, the outputs are not
+ * valid (dcp_mla_decode still merges them), and the kernel exits after about
+ * 40 ms per wave of CTAs, leaving the context usable. A CTA whose split holds
+ * no token writes its zero output and never waits.
+ */
+#define DCP_MLA_FLAG_TEST_STALL 32u
 /*
  * DCP_FLAG_PREFETCH (8, include/dcp_lse_reduce.h) is also taken by the
  * producer: each CTA of the tcgen05 kernel brings Q and its split's first KV

@@ -131,6 +131,8 @@ def test_mla_producer_rejects_bad_arguments(lib):
     assert call(n_split=0) == -103 and call(n_split=17) == -103
     assert call(q=FAKE + 8) == -104 and call(kv_len=FAKE + 2) == -104 and call(o=arr(FAKE + 4, FAKE)) == -104
     assert call(flags=16) == -105 and call(flags=6) == -105  # the one-kernel flag is dcp_mla_decode's only
+    assert call(flags=64) == -105
+    assert call(flags=dcp.DCP_MLA_FLAG_TEST_STALL | dcp.DCP_MLA_FLAG_MMA_SYNC, B=0) == 0  # the stall test is known
     assert call(flags=dcp.DCP_FLAG_PREFETCH | dcp.DCP_FLAG_PDL, B=0) == 0  # the producer takes the prefetch flag
     assert call(B=0) == 0  # nothing to do, nothing launched
     assert dcp.dcp_mla_decode_smem_bytes(576, 64) > 150000
@@ -185,6 +187,7 @@ def test_producer_kernel_choice(lib):
     # forcing flags (PDL does not change the choice)
     assert k(16, 64, 1, dcp.DCP_MLA_FLAG_TCGEN05) == tc and k(128, 1 << 20, 1, dcp.DCP_MLA_FLAG_MMA_SYNC) == mma
     assert k(128, 4096, 1, dcp.DCP_FLAG_PDL) == tc and k(128, 4096, 1, dcp.DCP_FLAG_PREFETCH) == tc
+    assert k(128, 4096, 1, dcp.DCP_MLA_FLAG_TEST_STALL) == tc and k(16, 64, 1, dcp.DCP_MLA_FLAG_TEST_STALL) == mma
     for args, status in [((128, 4096, 1, dcp.DCP_MLA_FLAG_TCGEN05 | dcp.DCP_MLA_FLAG_MMA_SYNC), -105),
                          ((128, 4096, 1, 16), -105), ((128, 4096, 0), -103), ((128, 4096, 17), -103),
                          ((20, 4096, 1), -102), ((128, -1, 1), -102)]:
@@ -249,4 +252,4 @@ def test_no_alloc_reports_bad_shapes_before_the_scratch_limit(lib):
     assert lib.dcp_mla_decode(FAKE, ptrs, ptrs, 8, 0, 128, 576, 512, 100, 0.1, 1, 2, FAKE, 1 << 20, ptrs, None, None,
                               dcp.DCP_MLA_FLAG_ONE_KERNEL | dcp.DCP_FLAG_PDL, None) == 0
     assert lib.dcp_mla_decode(FAKE, ptrs, ptrs, 8, 0, 128, 576, 512, 100, 0.1, 1, 2, FAKE, 1 << 20, ptrs, None, None,
-                              32, None) == -105
+                              64, None) == -105

@@ -500,3 +500,77 @@ def test_one_kernel_decode_matches_attention_and_replays_in_a_graph(oracle_mod):
         g.replay()
     torch.cuda.synchronize()
     assert all(torch.equal(a, b) for a, b in zip(ref, outs + louts))
+
+
+@pytest.mark.parametrize("kflags", KERNELS)
+def test_a_wait_that_never_completes_gives_up_and_reports(oracle_mod, kflags):
+    """The bounded waits, exercised on the GPU without a fault: with the stall
+    test flag every CTA arms its first KV tile's barrier for 16 bytes that
+    never arrive. Each such wait gives up after 20 ms, the status word reads 1,
+    the call ends (no hang, well under the two-second limit of a normal call),
+    a CTA whose range is empty still writes its zero output, and the context
+    stays usable: the same call without the flag then matches the oracle."""
+    import time
+
+    B, H, T, n_split = 3, 64, 600, 2
+    q, kv = make_mla_inputs(B, H, T, 576, seed=11)
+    lens = np.array([T, 0, 300], dtype=np.int32)
+    qd, kvd, ld = dev_bf16(q), dev_bf16(kv), torch.from_numpy(lens).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    outs, lses = dcp.mla_decode_partial(qd, kvd, ld, MLA_SCALE, n_split=n_split, status=status,
+                                        flags=kflags | dcp.DCP_MLA_FLAG_TEST_STALL)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(status.item()) == 1
+    assert elapsed < 1.5, f"the stalled call took {elapsed:.2f} s"
+    for s in range(n_split):
+        assert (outs[s][1] == 0).all() and (lses[s][1] == -float("inf")).all()
+
+    status.zero_()
+    outs, lses = dcp.mla_decode_partial(qd, kvd, ld, MLA_SCALE, n_split=n_split, status=status, flags=kflags)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_o, ref_l = oracle_partials(q, kv, lens, n_split, MLA_SCALE, True)
+    for s in range(n_split):
+        check_out(outs[s], ref_o[s], f"split {s} after a stalled call")
+        check_lse(lses[s], ref_l[s], f"split {s} after a stalled call")
+
+
+@pytest.mark.parametrize("one_kernel", [False, True])
+def test_fused_decode_after_a_stalled_producer(oracle_mod, one_kernel):
+    """dcp_mla_decode with the stall test flag: the producer's waits give up,
+    the status word reads 1 and the call ends, with the merge as a second
+    launch or, with the one-kernel flag, after the grid-wide sync that every
+    CTA of an aborted producer still reaches. A normal call follows and
+    matches attention over the whole context."""
+    from oracle.attention import attention
+
+    cp, n_split, B, H, T = 2, 2, 2, 64, 512
+    q, kv0 = make_mla_inputs(B, H, T, 576, seed=21)
+    _, kv1 = make_mla_inputs(B, H, T, 576, seed=22)
+    lens = [np.array([T, 200], dtype=np.int32), np.array([300, 0], dtype=np.int32)]
+    qd = dev_bf16(q)
+    kvs = [dev_bf16(kv0), dev_bf16(kv1)]
+    lds = [torch.from_numpy(x).cuda() for x in lens]
+    extra = dcp.DCP_MLA_FLAG_ONE_KERNEL if one_kernel else 0
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dcp.mla_decode_dcp(qd, kvs, lds, MLA_SCALE, n_split=n_split, status=status,
+                       flags=dcp.DCP_MLA_FLAG_TCGEN05 | dcp.DCP_MLA_FLAG_TEST_STALL | extra)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+
+    status.zero_()
+    outs, lse_outs = dcp.mla_decode_dcp(qd, kvs, lds, MLA_SCALE, n_split=n_split, status=status,
+                                        flags=dcp.DCP_MLA_FLAG_TCGEN05 | extra)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    qf, kvf = widen(q), [widen(kv0), widen(kv1)]
+    Hl = H // cp
+    for b in range(B):
+        ctx = np.concatenate([kvf[j][b, :lens[j][b]] for j in range(cp)], axis=0)
+        o, l = attention(qf[b:b + 1], ctx, MLA_SCALE, True, 512)
+        for r in range(cp):
+            check_out(outs[r][b], o[0, r * Hl:(r + 1) * Hl], f"row {b} dest {r}", kind="fused decode")
+            check_lse(lse_outs[r][b], l[0, r * Hl:(r + 1) * Hl], f"row {b} dest {r}", kind="fused decode")
