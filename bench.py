@@ -408,6 +408,49 @@ def stress_extra(peak, flags, sample_rows: int = 32):
              "parity_sample_rows": sample_rows}, sample)
 
 
+def timed_outputs_sample(sets):
+    """What the timed graphs left in their output buffers: per row count,
+    whether all of its calls' outputs are bit-identical (every call reads its
+    own copy of the same inputs), and host copies of the first and the last
+    call's outputs for the oracle check in the CPU-baseline leg."""
+    import torch
+    identical = True
+    sample = {}
+    for rows, rs in sets.items():
+        for d in rs.dst + rs.lse_out:
+            v = d.view(torch.int16) if d.dtype == torch.bfloat16 else d.view(torch.int32)
+            identical &= bool((v == v[0:1]).all())
+        sample[rows] = {k: ([d[k].float().double().cpu().numpy() for d in rs.dst],
+                            [l[k].double().cpu().numpy() for l in rs.lse_out]) for k in (0, rs.slots - 1)}
+    return {"calls_bit_identical": identical, "sample": sample}
+
+
+def timed_outputs_parity(cfg, timed):
+    """The first and the last call of every timed graph against the oracle on
+    the same seeded inputs, at the parity tests' tolerances."""
+    import oracle
+    from decode_context_mla_dcp_gb300.inputs import make_merge_inputs
+    worst_out = worst_lse = 0.0
+    ok = bool(timed["calls_bit_identical"])
+    for rows, by_call in timed["sample"].items():
+        inp = make_merge_inputs(cfg, rows, seed=0)
+        ref, lref = oracle.merge(inp.srcs, inp.lses, inp.lse_base_e)
+        for outs, louts in by_call.values():
+            for go, gl, ro, rl in zip(outs, louts, ref, lref):
+                err = np.abs(go - ro)
+                ok &= bool((err <= 1e-2 + 8e-3 * np.abs(ro)).all()) and not bool(np.isnan(go).any())
+                worst_out = max(worst_out, float(err.max()))
+                fin = np.isfinite(rl)
+                ok &= bool(np.array_equal(np.isfinite(gl), fin))
+                lerr = np.abs(gl[fin] - rl[fin]) / np.maximum(np.abs(rl[fin]), 1.0)
+                if lerr.size:
+                    ok &= bool((lerr <= 1e-5).all())
+                    worst_lse = max(worst_lse, float(lerr.max()))
+    return {"ok": ok, "calls_checked": "the first and the last of each row count's 60-call graph, as left by the "
+                                       "timed steps", "calls_bit_identical": bool(timed["calls_bit_identical"]),
+            "max_abs_err_out": worst_out, "max_rel_err_lse": worst_lse}
+
+
 def stress_sample_parity(sample):
     """The stress call's sampled rows (inputs and GPU outputs of the timed
     launch) against the oracle, at the parity tests' tolerances."""
@@ -825,6 +868,7 @@ def run_ours(args):
         dist.barrier()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
+    timed = timed_outputs_sample(sets) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
 
     step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)]
     per_rows_us = {rows: statistics.median(evs[k][i].elapsed_time(evs[k][i + 1]) * 1e3 / CALLS_PER_GRAPH
@@ -881,6 +925,8 @@ def run_ours(args):
         out["cpu_baseline"] = cpu_baseline(cfg)
         if stress_sample is not None:
             out["cpu_baseline"]["parity_vs_oracle"]["stress_sample"] = stress_sample_parity(stress_sample)
+        if timed is not None:
+            out["cpu_baseline"]["parity_vs_oracle"]["timed_calls"] = timed_outputs_parity(cfg, timed)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
