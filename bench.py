@@ -959,6 +959,23 @@ def run_case(args):
         torch.cuda.synchronize()
         print(f"case mla x {args.calls} calls done", flush=True)
         return 0
+    if args.case == "fused":
+        # the fused decode as the bench times it: 8 rows x 128 heads, cp = 8 shards of 512 tokens, one split
+        # per shard, PDL and the producer's L2 prefetch; each call on its own caches
+        from decode_context_mla_dcp_gb300.inputs import MLA_SCALE
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(0)
+        B, H, cp, Ts = 8, 128, 8, 512
+        q = torch.randn((B, H, 576), generator=gen, device="cuda").to(torch.bfloat16)
+        lens = [torch.full((B,), Ts, dtype=torch.int32, device="cuda") for _ in range(cp)]
+        caches = [[torch.randn((B, Ts, 576), generator=gen, device="cuda").to(torch.bfloat16) for _ in range(cp)]
+                  for _ in range(args.calls)]
+        torch.cuda.synchronize()
+        for kvs in caches:
+            dcp.mla_decode_dcp(q, kvs, lens, MLA_SCALE, n_split=1, flags=dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH)
+        torch.cuda.synchronize()
+        print(f"case fused x {args.calls} calls done", flush=True)
+        return 0
     cfg = CONFIGS[args.case]
     rows_list = [int(r) for r in args.rows.split(",")] if args.rows else list(cfg.rows)
     flags = dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH
@@ -993,7 +1010,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the L2-hot, no-PDL and stress extras")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["kimi", "deepseek", "spec", "stress", "mla"],
+    ap.add_argument("--case", choices=["kimi", "deepseek", "spec", "stress", "mla", "fused"],
                     help="profiling mode: plain calls of one config, no timing")
     ap.add_argument("--rows", default="", help="with --case: comma-separated row counts")
     ap.add_argument("--calls", type=int, default=3, help="with --case: calls per row count")
