@@ -946,7 +946,8 @@ def run_case(args):
     dcp_build.build()
     if args.case == "mla":
         # the producer on a DeepSeek-V2-shaped shard, as the bench times it: 8 rows x 128 heads x 4096
-        # tokens, 9 splits (one wave), PDL and the L2 prefetch
+        # tokens, 9 splits (one wave), PDL and the L2 prefetch (--mla-kernel / --mla-splits change the
+        # kernel and the split count)
         from decode_context_mla_dcp_gb300.inputs import MLA_SCALE
         gen = torch.Generator(device="cuda")
         gen.manual_seed(0)
@@ -954,8 +955,10 @@ def run_case(args):
         q = torch.randn((B, H, 576), generator=gen, device="cuda").to(torch.bfloat16)
         kvs = [torch.randn((B, T, 576), generator=gen, device="cuda").to(torch.bfloat16) for _ in range(args.calls)]
         lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+        kflags = {"auto": 0, "tcgen05": dcp.DCP_MLA_FLAG_TCGEN05, "mma_sync": dcp.DCP_MLA_FLAG_MMA_SYNC}[args.mla_kernel]
         for kv in kvs:
-            dcp.mla_decode_partial(q, kv, lens, MLA_SCALE, n_split=9, flags=dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH)
+            dcp.mla_decode_partial(q, kv, lens, MLA_SCALE, n_split=args.mla_splits,
+                                   flags=dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH | kflags)
         torch.cuda.synchronize()
         print(f"case mla x {args.calls} calls done", flush=True)
         return 0
@@ -1014,6 +1017,9 @@ def main(argv=None):
                     help="profiling mode: plain calls of one config, no timing")
     ap.add_argument("--rows", default="", help="with --case: comma-separated row counts")
     ap.add_argument("--calls", type=int, default=3, help="with --case: calls per row count")
+    ap.add_argument("--mla-kernel", choices=["auto", "tcgen05", "mma_sync"], default="auto",
+                    help="with --case mla: the producer kernel")
+    ap.add_argument("--mla-splits", type=int, default=9, help="with --case mla: splits per row")
     ap.add_argument("--schedule", choices=["default", "lse_first"], default="default",
                     help="with --case (merge configs): the merge schedule")
     args = ap.parse_args(argv)
