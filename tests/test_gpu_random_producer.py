@@ -52,3 +52,39 @@ def test_random_producer_calls_match_the_oracle(oracle_mod, case):
     for s in range(n_split):
         check_out(outs[s], ref_o[s], f"split {s}, {what}")
         check_lse(lses[s], ref_l[s], f"split {s}, {what}")
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_random_fused_decodes_match_full_attention(oracle_mod, case):
+    """dcp_mla_decode on random shard counts, splits, heads and row lengths
+    (the context interleaved token by token over the shards), the two-launch
+    default and the one-kernel flag, against fp64 attention over each row's
+    whole context."""
+    from oracle.attention import attention
+    from tests.test_gpu_mla import _interleaved_shards, widen
+
+    rng = np.random.default_rng([88, case])
+    cp = int(rng.choice([1, 2, 4, 8]))
+    n_split = int(rng.integers(1, 16 // cp + 1))
+    Hs = 16 * int(rng.integers(1, 3))                 # heads per (shard, split) block of the merge
+    H = Hs * cp * n_split if Hs * cp * n_split <= 192 else 16 * cp * n_split
+    Dk = int(rng.choice([512, 576]))
+    B = int(rng.integers(1, 5))
+    L_max = int(rng.integers(1, 700))
+    L = rng.integers(0, L_max + 1, size=B).astype(np.int32)
+    L[0] = L_max
+    flags = int(rng.choice([0, dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH])) | \
+        (dcp.DCP_MLA_FLAG_ONE_KERNEL if case % 2 else 0)
+    q, kv_full = make_mla_inputs(B, H, L_max, Dk, seed=2000 + case)
+    kvs, lens = _interleaved_shards(kv_full, L, cp)
+    outs, louts = dcp.mla_decode_dcp(dev_bf16(q), kvs, lens, MLA_SCALE, n_split=n_split, flags=flags)
+    torch.cuda.synchronize()
+    what = f"cp={cp} n_split={n_split} H={H} Dk={Dk} B={B} L={L.tolist()} flags={flags}"
+    Hl = H // cp
+    for b in range(B):
+        o_ref, l_ref = attention(widen(q[b:b + 1]), widen(kv_full[b, :L[b]]), MLA_SCALE, dv=512)
+        for r in range(cp):
+            check_out(outs[r][b:b + 1], o_ref[:, r * Hl:(r + 1) * Hl], f"row {b} dest {r}, {what}",
+                      kind="fused decode")
+            check_lse(louts[r][b:b + 1], l_ref[:, r * Hl:(r + 1) * Hl], f"row {b} dest {r}, {what}",
+                      kind="fused decode")
