@@ -2,8 +2,17 @@
 // of the DCP partial outputs and LSEs. What it computes, and the passages it
 // follows, are stated in include/dcp_mla_decode.h.
 //
-// Design. One CTA owns (split s, a block of 16*kG heads, row b) and walks its
-// token range in tiles of 32 tokens:
+// The file holds two kernels and their host side:
+//   * mla_partial_kernel, on the warp-level mma.sync tensor path (below);
+//   * mla_partial_tc_kernel, on the 5th-generation tensor cores (tcgen05 MMA
+//     into TMEM, operands loaded by TMA; its design is stated before it);
+//   * the host entry points: the producer (which picks a kernel), the fused
+//     DCP decode (producer over every shard, then the merge of
+//     dcp_lse_reduce.cu, or with DCP_MLA_FLAG_ONE_KERNEL the merge inside the
+//     producer's launch) and its form that allocates nothing.
+//
+// Design of the mma.sync kernel. One CTA owns (split s, a block of 16*kG
+// heads, row b) and walks its token range in tiles of 32 tokens:
 //   * Q for the head block and each KV tile land in shared memory by 1-D bulk
 //     asynchronous copies (cp.async.bulk, one per row, completing on an
 //     mbarrier), into rows padded by 16 bytes so that the 8x8 ldmatrix reads
