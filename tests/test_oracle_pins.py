@@ -406,6 +406,18 @@ def test_attention_two_tokens_closed_form():
     np.testing.assert_allclose(lse[0, 0], math.log(4.0), rtol=1e-15)
 
 
+def test_attention_is_stable_for_widely_spread_scores():
+    # scores 0 and 1000: exp(-1000) underflows to 0, so the second token takes
+    # all the weight (o = its row exactly) and lse = 1000; taking the maximum
+    # out before exponentiating is what keeps exp(1000) from overflowing
+    from oracle.attention import attention
+    q = np.zeros((1, 1, 4)); q[0, 0, 0] = 1.0
+    kv = np.array([[0.0, 1.0, 2.0, 3.0], [1000.0, 5.0, -2.0, 7.0]])
+    o, lse = attention(q, kv, 1.0, dv=4)
+    assert np.array_equal(o[0, 0], kv[1])
+    assert lse[0, 0] == 1000.0
+
+
 def test_attention_is_invariant_under_token_permutation():
     from oracle.attention import attention
     rng = np.random.default_rng(55)
