@@ -504,3 +504,41 @@ def test_runs_on_a_side_stream_in_order():
             o, _ = dcp.merge(srcs, lses, False, flags=dcp.DCP_FLAG_PDL)
     s.synchronize()
     assert all(torch.equal(a, b) for a, b in zip(_bits(ref_o), _bits(o)))
+
+
+def test_batch_beyond_one_launch_is_split_and_exact():
+    """The largest batch the merge takes in one launch is 2^30 (row, head)
+    units; a larger one runs as several launches over row ranges. Here cp = 2,
+    H = 16 (8 per destination), D = 8 and 2^26 + 3 rows: 2^30 + 48 units, two
+    launches, about 60 GiB of buffers. Both sources have the same LSE, so each
+    weight is exactly 1/2 and the output is the bf16 rounding of the exact
+    mean, the merged LSE lse + ln 2 in fp32; checked bit for bit everywhere,
+    on the device, in row chunks."""
+    free, _ = torch.cuda.mem_get_info()
+    if free < (72 << 30):
+        pytest.skip("needs about 60 GiB of free device memory")
+    cp, H, D = 2, 16, 8
+    Hl = H // cp
+    B = (1 << 26) + 3
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(11)
+    chunk = 1 << 22
+    srcs = [torch.empty((B, H, D), dtype=torch.bfloat16, device="cuda") for _ in range(cp)]
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    for b0 in range(0, B, chunk):
+        b1 = min(B, b0 + chunk)
+        for s in srcs:
+            s[b0:b1] = torch.randn((b1 - b0, H, D), generator=gen, device="cuda").to(torch.bfloat16)
+        lse[b0:b1] = torch.randn((b1 - b0, H), generator=gen, device="cuda") * 6.0 + 10.0
+    lses = [lse, lse.clone()]
+    outs, louts = dcp.merge(srcs, lses, True)
+    torch.cuda.synchronize()
+    ln2 = torch.tensor(0.6931471805599453, dtype=torch.float32, device="cuda")
+    for b0 in range(0, B, chunk):
+        b1 = min(B, b0 + chunk)
+        for r in range(cp):
+            h = slice(r * Hl, (r + 1) * Hl)
+            want = ((srcs[0][b0:b1, h].float() + srcs[1][b0:b1, h].float()) * 0.5).to(torch.bfloat16)
+            assert torch.equal(outs[r][b0:b1].view(torch.int16), want.view(torch.int16)), f"rows {b0}.. dest {r}"
+            want_l = lse[b0:b1, h] + ln2
+            assert torch.equal(louts[r][b0:b1].view(torch.int32), want_l.view(torch.int32)), f"LSE rows {b0}.. {r}"
