@@ -574,3 +574,32 @@ def test_fused_decode_after_a_stalled_producer(oracle_mod, one_kernel):
         for r in range(cp):
             check_out(outs[r][b], o[0, r * Hl:(r + 1) * Hl], f"row {b} dest {r}", kind="fused decode")
             check_lse(lse_outs[r][b], l[0, r * Hl:(r + 1) * Hl], f"row {b} dest {r}", kind="fused decode")
+
+
+@pytest.mark.parametrize("H,T,kflags", [(16, 5, dcp.DCP_MLA_FLAG_MMA_SYNC), (64, 128, dcp.DCP_MLA_FLAG_TCGEN05)])
+def test_producer_at_the_largest_batch(oracle_mod, H, T, kflags):
+    """B = 65535 rows, the producer's largest batch (one grid row per batch
+    row): every row is computed (LSEs finite where the row has tokens, -inf
+    where it has none), and sampled rows, the last ones included, match the
+    oracle attention. Inputs are drawn on the device by a seeded generator;
+    the sampled rows are copied to the host for the oracle."""
+    B, Dk = 65535, 576
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(H + T)
+    q = torch.randn((B, H, Dk), generator=gen, device="cuda").to(torch.bfloat16)
+    kv = torch.randn((B, T, Dk), generator=gen, device="cuda").to(torch.bfloat16)
+    lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    lens[::7] = 0
+    outs, lses = dcp.mla_decode_partial(q, kv, lens, MLA_SCALE, n_split=1, flags=kflags)
+    torch.cuda.synchronize()
+    empty = lens == 0
+    assert torch.isfinite(lses[0][~empty]).all() and (lses[0][empty] == -float("inf")).all()
+    assert not torch.isnan(outs[0].float()).any()
+    rows = [1, 2, 1000, 40001, B - 2, B - 1]
+    for b in rows:
+        qb = q[b:b + 1].view(torch.int16).cpu().numpy().view(np.uint16)
+        kvb = kv[b:b + 1].view(torch.int16).cpu().numpy().view(np.uint16)
+        lb = lens[b:b + 1].cpu().numpy()
+        ref_o, ref_l = oracle_partials(qb, kvb, lb, 1, MLA_SCALE, True)
+        check_out(outs[0][b:b + 1], ref_o[0], f"row {b}")
+        check_lse(lses[0][b:b + 1], ref_l[0], f"row {b}")
