@@ -603,3 +603,49 @@ def test_producer_at_the_largest_batch(oracle_mod, H, T, kflags):
         ref_o, ref_l = oracle_partials(qb, kvb, lb, 1, MLA_SCALE, True)
         check_out(outs[0][b:b + 1], ref_o[0], f"row {b}")
         check_lse(lses[0][b:b + 1], ref_l[0], f"row {b}")
+
+
+def test_concurrent_callers_on_their_own_streams():
+    """Two host threads call the producer, the fused decode and the merge at
+    the same time, each on its own stream (ctypes releases the GIL during a
+    call, so the library runs concurrently on both). Every result equals the
+    single-threaded one bit for bit."""
+    import threading
+
+    B, H, T, cp = 3, 64, 600, 2
+    q, kv = make_mla_inputs(B, H, T, 576, seed=31)
+    qd, kvd = dev_bf16(q), dev_bf16(kv)
+    lens = torch.tensor([T, 300, 0], dtype=torch.int32, device="cuda")
+    shard_lens = [lens, torch.tensor([T, 1, 0], dtype=torch.int32, device="cuda")]
+
+    def work(stream):
+        with torch.cuda.stream(stream):
+            o, l = dcp.mla_decode_partial(qd, kvd, lens, MLA_SCALE, n_split=2, stream=stream)
+            fo, fl = dcp.mla_decode_dcp(qd, [kvd, kvd], shard_lens, MLA_SCALE, n_split=2, stream=stream)
+            mo, ml = dcp.merge(o, l, True, stream=stream)
+        stream.synchronize()
+        return [x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32) for x in o + l + fo + fl + mo + ml]
+
+    torch.cuda.synchronize()  # inputs in place before other streams read them
+    ref = work(torch.cuda.Stream())
+    results, errors = {}, []
+
+    def run(k):
+        try:
+            s = torch.cuda.Stream()
+            for it in range(20):
+                got = work(s)
+                if not all(torch.equal(a, b) for a, b in zip(ref, got)):
+                    results[k] = f"mismatch at iteration {it}"
+                    return
+            results[k] = "ok"
+        except Exception as e:  # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=run, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    assert results == {0: "ok", 1: "ok"}, results
