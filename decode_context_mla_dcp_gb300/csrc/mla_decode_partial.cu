@@ -1015,13 +1015,14 @@ __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc
             // so each lane converts and stores two dims of one head in one word
             const bool odd = (lane & 1) != 0;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int dv = 128 * m + 32 * quad + (lane & ~1);  // the pair's first dim
+            for (int j = 0; j < kHW; j += 2) {
+                const float2 inv = *reinterpret_cast<const float2*>(a_s + hb + j);  // read once per head pair
+                const int hh = hb + j + (odd ? 1 : 0);
 #pragma unroll
-                for (int j = 0; j < kHW; j += 2) {
-                    const float x0 = ov[m][j] * a_s[hb + j], x1 = ov[m][j + 1] * a_s[hb + j + 1];
+                for (int m = 0; m < 4; ++m) {
+                    const int dv = 128 * m + 32 * quad + (lane & ~1);  // the pair's first dim
+                    const float x0 = ov[m][j] * inv.x, x1 = ov[m][j + 1] * inv.y;
                     const float got = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
-                    const int hh = hb + j + (odd ? 1 : 0);
                     *reinterpret_cast<__nv_bfloat162*>(o_s + hh * kDv + dv) =
                         odd ? __floats2bfloat162_rn(got, x1) : __floats2bfloat162_rn(x0, got);
                 }
