@@ -649,3 +649,31 @@ def test_concurrent_callers_on_their_own_streams():
         t.join(timeout=120)
     assert not errors, errors
     assert results == {0: "ok", 1: "ok"}, results
+
+
+@pytest.mark.parametrize("kflags", KERNELS)
+def test_empty_cache_gives_zero_outputs_and_neg_inf(kflags):
+    """T = 0 (a cache that holds no tokens for any row): every split writes
+    output 0 and LSE -inf, whatever the token counts say (they clamp to 0).
+    And a fused decode in which one shard has no tokens for any row equals
+    the producer over the other shard alone, bit for bit (weights 0 and 1)."""
+    B, H = 3, 64
+    q, kv = make_mla_inputs(B, H, 300, 576, seed=41)
+    qd, kvd = dev_bf16(q), dev_bf16(kv)
+    lens = torch.tensor([5, 0, 100], dtype=torch.int32, device="cuda")
+    outs = [torch.full((B, H, 512), 7.0, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    lses = [torch.zeros((B, H), dtype=torch.float32, device="cuda") for _ in range(2)]
+    # the C entry point with T = 0 (the cache pointer is valid but no row of it is read)
+    dcp.dcp_mla_decode_partial(qd, kvd, lens, B, H, 576, 512, 0, MLA_SCALE, True, 2, outs, lses, flags=kflags)
+    torch.cuda.synchronize()
+    for s_ in range(2):
+        assert (outs[s_] == 0).all() and (lses[s_] == -float("inf")).all()
+
+    none = torch.zeros((B,), dtype=torch.int32, device="cuda")
+    full = torch.full((B,), 300, dtype=torch.int32, device="cuda")
+    _, kv2 = make_mla_inputs(B, H, 300, 576, seed=42)
+    both, both_l = dcp.mla_decode_dcp(qd, [dev_bf16(kv2), kvd], [none, full], MLA_SCALE, n_split=1, flags=kflags)
+    alone, alone_l = dcp.mla_decode_partial(qd, kvd, full, MLA_SCALE, n_split=1, flags=kflags)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(both, dim=1).view(torch.int16), alone[0].view(torch.int16))
+    assert torch.equal(torch.cat(both_l, dim=1).view(torch.int32), alone_l[0].view(torch.int32))
