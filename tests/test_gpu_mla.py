@@ -677,3 +677,28 @@ def test_empty_cache_gives_zero_outputs_and_neg_inf(kflags):
     torch.cuda.synchronize()
     assert torch.equal(torch.cat(both, dim=1).view(torch.int16), alone[0].view(torch.int16))
     assert torch.equal(torch.cat(both_l, dim=1).view(torch.int32), alone_l[0].view(torch.int32))
+
+
+@pytest.mark.parametrize("flags", [dcp.DCP_FLAG_PDL | dcp.DCP_FLAG_PREFETCH, dcp.DCP_MLA_FLAG_ONE_KERNEL,
+                                   dcp.DCP_MLA_FLAG_MMA_SYNC])
+def test_no_alloc_decode_is_bit_identical_to_the_workspace_decode_under_each_flag(flags):
+    """The built-in scratch only replaces the caller's workspace: with the
+    launch flags, the one-kernel form and the mma.sync producer, the
+    no-allocation decode gives the same bits as dcp_mla_decode."""
+    cp, n_split, B, H, T = 2, 2, 3, 64, 300
+    q, kv0 = make_mla_inputs(B, H, T, 576, seed=61)
+    _, kv1 = make_mla_inputs(B, H, T, 576, seed=62)
+    qd, kvs = dev_bf16(q), [dev_bf16(kv0), dev_bf16(kv1)]
+    lens = [torch.tensor([T, 17, 0], dtype=torch.int32, device="cuda"),
+            torch.tensor([200, 0, 0], dtype=torch.int32, device="cuda")]
+    ws = torch.empty((dcp.dcp_mla_decode_workspace_bytes(cp, n_split, B, H),), dtype=torch.uint8, device="cuda")
+    outs = [[torch.empty((B, H // cp, 512), dtype=torch.bfloat16, device="cuda") for _ in range(cp)] for _ in range(2)]
+    louts = [[torch.empty((B, H // cp), dtype=torch.float32, device="cuda") for _ in range(cp)] for _ in range(2)]
+    dcp.dcp_mla_decode(qd, kvs, lens, cp, B, H, 576, 512, T, MLA_SCALE, True, n_split, ws, ws.numel(), outs[0],
+                       louts[0], flags=flags)
+    dcp.dcp_mla_decode_noalloc(qd, kvs, lens, cp, B, H, 576, 512, T, MLA_SCALE, True, n_split, outs[1], louts[1],
+                               flags=flags)
+    torch.cuda.synchronize()
+    for r in range(cp):
+        assert torch.equal(outs[0][r].view(torch.int16), outs[1][r].view(torch.int16))
+        assert torch.equal(louts[0][r].view(torch.int32), louts[1][r].view(torch.int32))
