@@ -464,8 +464,8 @@ __global__ void __launch_bounds__(128 * kG, 1) mla_partial_kernel(const __grid_c
 // slices serve as the K-major A operand of the scores and, read along the
 // latent dims, as the M-major A operand of the values. TMEM holds S^T (kNH
 // columns) and O^T (4 x kNH columns). A thread owns one token of the tile and
-// its heads (all kNH of them, or half when kNH >= 32: then warp w reads TMEM
-// lane quadrant w % 4 for head half w / 4). The per-head maxima over the tile
+// its heads (all kNH of them, or a quarter when kNH >= 32: then warp w reads
+// TMEM lane quadrant w % 4 for head quarter w / 4). The per-head maxima over the tile
 // come from a reduce-scatter butterfly across lanes and shared memory, and the
 // running maximum moves only when a head's tile maximum exceeds it by more
 // than 2^8 (then O^T is rescaled in TMEM), so the rescale is rare. P^T (bf16)
@@ -709,9 +709,12 @@ __device__ __noinline__ void merge_partials(const TcParams& p, int64_t B) {
 }
 
 // Threads of the tcgen05 kernel: one per (token, group of heads); with 32 or
-// more heads per CTA each token's heads are split over two threads.
+// more heads per CTA each token's heads are split over four threads (512
+// threads, at most 128 registers each). The softmax and the epilogue are
+// latency chains over a thread's heads, so shorter chains on more warps run
+// faster; eight groups would spill.
 template <int kNH>
-__host__ __device__ constexpr int tc_head_groups() { return kNH >= 32 ? 2 : 1; }
+__host__ __device__ constexpr int tc_head_groups() { return kNH >= 32 ? 4 : 1; }
 
 template <int kDk, int kNH>
 __global__ void __launch_bounds__(128 * tc_head_groups<kNH>(), 1) mla_partial_tc_kernel(const __grid_constant__ TcParams p) {
